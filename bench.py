@@ -1,0 +1,454 @@
+"""Benchmark: one paged-KV decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: kv_cache_append of
+this step's token for every sequence (slot scatter), then paged_attn_decode
+(block-table gather, TMA staging of K/V blocks, fused QK / online softmax / PV,
+split-KV partials and the cross-split reduce).  The default workload is the
+Llama-7B-shaped MHA decode batch (64 sequences, 32 q/kv heads, head_dim 128,
+block_size 16, fp16, context lengths uniform in [512, 4096], blocks shuffled
+over a 16384-block pool), with seeded synthetic inputs.
+
+Prints ONE JSON line (rank 0).  `value` is decode-attention KV-read GB/s of the
+whole job: algorithmic K+V bytes (sum_i L_i * Hkv * D * 2 * 2 per step, all
+ranks) / max-over-ranks time of the timed steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    (N > 1: launch under torch.distributed.run; every rank runs an
+     independent replica of the batch, no collective on the data path)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from dataclasses import replace
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_268_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode-attention KV-read GB/s and % of GB300 HBM peak; seq-tokens/s"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "llama7b_mha"
+FALLBACK_HBM_GBS = 6800.0
+DTYPE_NAME = {W.F16: "f16", W.BF16: "bf16"}
+
+
+# ---------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.ORDER)
+    p.add_argument("--num-seqs", type=int, default=0,
+                   help="shrink the batch (and pool) for profiler captures; 0 = full workload")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--split-tokens", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_cache_268_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None when missing or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = j.get(workload)
+    if not entry or entry.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_full_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampler (started before, stopped after the
+    timed region); keeps host timestamps so samples can be cut to the region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.proc:
+            return None
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [p for t, p in self.samples if t <= t1]
+            window = "warmup+timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for p in inside for k in range(4) if p[5 + k].lower() == "active"})
+        power = [num(p[3]) for p in inside if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- workload
+def build_workload(args, rank: int, device):
+    spec = W.WORKLOADS[args.workload]
+    if args.num_seqs and args.num_seqs != spec.num_seqs:
+        # same length distribution, heads and pool density; fewer sequences
+        n = args.num_seqs
+        largs = spec.len_args[:n] if spec.lens == "fixed" else spec.len_args
+        spec = replace(spec, name=f"{spec.name}/{n}", num_seqs=n, len_args=largs,
+                       num_blocks=max(64, -(-spec.num_blocks * n // spec.num_seqs)))
+    return W.make(spec, seed=args.seed + rank, device=device)
+
+
+def oracle_sample_rate(w: W.Workload, target_s: float, device, seed: int = 0):
+    """Time the CPU oracle on a bounded sample of (sequence, query head) rows of
+    the same workload; returns (GB/s of KV rows read, description)."""
+    import oracle  # test infrastructure: only the CPU-baseline / reference legs use it
+
+    spec = w.spec
+    rng = np.random.default_rng(seed)
+    # calibrate on one row of a median-length sequence
+    order = np.argsort(w.context_lens)
+    mid = int(order[len(order) // 2])
+
+    def compact(seqs):
+        # gather the referenced blocks of the sampled sequences into a small pool
+        seqs = np.asarray(seqs)
+        nblk = -(-w.context_lens[seqs] // spec.block_size)
+        ids = np.concatenate([w.block_tables[s, :n] for s, n in zip(seqs, nblk)])
+        uniq, inv = np.unique(ids, return_inverse=True)
+        idx = torch.from_numpy(uniq.astype(np.int64)).to(w.k_cache.device)
+        kc = W.bits(w.k_cache.index_select(0, idx))
+        vc = W.bits(w.v_cache.index_select(0, idx))
+        tables = np.full((len(seqs), w.block_tables.shape[1]), -1, dtype=np.int32)
+        k = 0
+        for r, n in enumerate(nblk):
+            tables[r, :n] = inv[k:k + n]
+            k += n
+        return kc, vc, tables
+
+    qb = W.bits(w.q)
+    kc, vc, t = compact([mid])
+    t0 = time.perf_counter()
+    oracle.decode_rows([(0, 0)], qb[[mid]], kc, vc, t, w.context_lens[[mid]], w.scale, spec.dtype)
+    per_row = max(time.perf_counter() - t0, 1e-4)
+    nrows = int(max(1, min(spec.num_seqs * spec.num_q_heads, target_s / per_row)))
+    flat = rng.choice(spec.num_seqs * spec.num_q_heads, size=nrows, replace=False)
+    seqs = np.unique(flat // spec.num_q_heads)
+    kc, vc, tables = compact(seqs)
+    remap = {int(s): r for r, s in enumerate(seqs)}
+    rows = np.array([(remap[int(f // spec.num_q_heads)], int(f % spec.num_q_heads)) for f in flat],
+                    dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.decode_rows(rows, qb[seqs], kc, vc, tables, w.context_lens[seqs], w.scale, spec.dtype)
+    dt = time.perf_counter() - t0
+    # KV bytes a row reads: its L tokens of K and V for one kv head, shared by G q heads
+    kv = sum(int(w.context_lens[seqs[r]]) for r, _ in rows) * spec.head_dim * 2 * 2 / spec.group
+    desc = (f"{nrows} of {spec.num_seqs * spec.num_q_heads} (sequence, q head) rows of "
+            f"{spec.name}, single-threaded fp64 C oracle, {dt:.1f} s")
+    return kv / dt / 1e9, desc, dt
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    spec = W.WORKLOADS[args.workload]
+    w = W.make(spec, seed=args.seed, device="cpu" if not torch.cuda.is_available() else "cuda")
+    nsteps = args.steps + args.warmup
+    per_step = max(0.5, min(args.cpu_seconds, 150.0 / max(nsteps, 1)))
+    rates, times = [], []
+    for i in range(nsteps):
+        gbs, desc, dt = oracle_sample_rate(w, per_step, None, seed=i)
+        if i >= args.warmup:
+            rates.append(gbs)
+            times.append(dt)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "num_seqs": spec.num_seqs,
+                   "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
+                   "head_dim": spec.head_dim, "block_size": spec.block_size,
+                   "element_type": DTYPE_NAME[spec.dtype], "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_pkv(args):
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from paged_kv_cache_268_gb300 import _binding as pkv
+    from paged_kv_cache_268_gb300 import build as pkv_build
+    if rank == 0 or not os.path.exists(pkv_build.LIB):
+        pkv_build.build()
+    if dist:
+        dist.barrier()
+    pkv.load_library()
+
+    w = build_workload(args, rank, dev)
+    spec = w.spec
+    q = w.q
+    kc, vc = w.k_cache, w.v_cache
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    k_new, v_new = w.k_new, w.v_new
+    out = torch.empty_like(q)
+    maxL = w.max_context_len
+    shape = pkv.decode_shape(q, kc, bt, maxL, args.split_tokens)
+    plan = pkv.decode_plan(shape)
+    ws_buf = pkv.alloc_workspace(shape, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
+        pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
+                              split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.2 if sampler else 0)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = pkv.launch_count()
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        a, b, c = ev[i]
+        a.record(stream)
+        pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
+        b.record(stream)
+        pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
+                              split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+        c.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    launches = pkv.launch_count() - n0
+    if dist:
+        dist.barrier()
+    if sampler:
+        sampler.stop()
+    total_ms = start.elapsed_time(end)
+    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    append_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert pkv.get_device_error() == 0
+
+    kv_bytes = w.kv_bytes()
+    ms_per_step = total_ms / K
+    value = ws * kv_bytes * K / (total_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    dec_avg = sum(decode_ms) / K
+    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
+
+    # end-to-end through the public API with pinned host buffers: per step,
+    # copy this step's inputs host->device, run append + decode, read out back
+    e2e = None
+    if not args.no_e2e:
+        h_q = q.cpu().pin_memory()
+        h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+        h_slots = slots.cpu().pin_memory()
+        h_bt, h_cl = bt.cpu().pin_memory(), cl.cpu().pin_memory()
+        h_out = torch.empty_like(h_q).pin_memory()
+        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+        d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_bt, h_bt), (d_cl, h_cl)):
+                d.copy_(h, non_blocking=True)
+            pkv.kv_cache_append(d_k, d_v, d_slots, kc, vc, stream=stream)
+            pkv.paged_attn_decode(d_q, kc, vc, d_bt, d_cl, w.scale, out, max_context_len=maxL,
+                                  split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(10, min(K, 500))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+        e2e = {"value": ws * kv_bytes * Ke / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+               "ms_per_step": e_ms / Ke}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        gbs, desc, _ = oracle_sample_rate(w, args.cpu_seconds, dev)
+        cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    traffic = recorded_traffic(spec.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[spec.dtype],
+        "data": "synthetic",
+        "config": {"workload": spec.name, "num_seqs": spec.num_seqs,
+                   "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
+                   "head_dim": spec.head_dim, "block_size": spec.block_size,
+                   "pool_blocks": spec.num_blocks, "context_lens": f"{spec.lens}{tuple(spec.len_args)}",
+                   "sum_context_len": int(w.context_lens.sum()), "seed": args.seed,
+                   "step": "kv_cache_append(1 token/seq) + paged_attn_decode",
+                   "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
+                   "kernel_variant": "mma" if plan.variant else "simt",
+                   "l2": f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "pct_hbm_peak": value / ws / peak,
+        "seq_tokens_per_s": ws * spec.num_seqs * K / (total_ms * 1e-3),
+        "context_tokens_per_s": ws * int(w.context_lens.sum()) * K / (total_ms * 1e-3),
+        "decode_ms_median": statistics.median(decode_ms),
+        "decode_ms_p90": float(np.percentile(decode_ms, 90)),
+        "append_us_median": 1e3 * statistics.median(append_ms),
+        "roofline": {"bound": "hbm", "kernel": "paged_attn_decode (decode + split reduce)",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_pkv(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+/*
+ * pkv — paged KV-cache decode attention for GB300 (sm_103a), C ABI.
+ *
+ * The problem these calls solve is stated in the "PagedAttention" section of
+ * the third page (bbs.pinggu.org thread 16345627, "memory management as an
+ * operating system"): the KV cache of every sequence is cut into fixed-size
+ * physical blocks that need not be contiguous in device memory, a per-sequence
+ * block table maps logical blocks to physical ones, and the attention kernel
+ * reaches K/V by looking the block up in the table (indirect addressing).  The
+ * attention itself is softmax(q . K^T * scale) . V (second page, "model
+ * executor" article, section 3.1); a decode step has one query token per
+ * sequence, so there is no mask.  New tokens enter the cache through the block
+ * manager's slots (first page, section 4.2) once per scheduler iteration
+ * (third page, "continuous batching").
+ *
+ * Conventions for every call
+ *  - All array arguments are DEVICE pointers owned by the caller; the library
+ *    never frees or retains them.  Layouts are dense and row-major.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream).  No call synchronises the host, except pkv_get_device_error.
+ *  - Calls return PKV_OK (0) or a negative PKV_ERR_* code.  Argument errors are
+ *    detected on the host before anything is enqueued.  The CONTENTS of device
+ *    arrays (block ids, slots, lengths) cannot be checked on the host without a
+ *    sync; the kernels check them instead, skip the offending unit and record
+ *    a code in a device-side error word read by pkv_get_device_error.
+ *  - Both calls are deterministic: the same inputs give bit-identical outputs.
+ *  - Calls enqueued on one stream run in order, so a decode enqueued after an
+ *    append on the same stream sees the appended tokens.
+ *
+ * Element type: q, k, v, k_cache, v_cache and out all share one 16-bit type,
+ * IEEE binary16 (PKV_F16) or bfloat16 (PKV_BF16).  Arithmetic is FP32 with
+ * round-to-nearest-even on the final store.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared here so that callers need no CUDA
+ * header. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+enum {
+  PKV_OK = 0,
+  PKV_ERR_NULL = -1,         /* a required pointer is NULL */
+  PKV_ERR_INVALID = -2,      /* a size is out of range, or Hq % Hkv != 0 */
+  PKV_ERR_UNSUPPORTED = -3,  /* head_dim, block_size, group size or dtype not built */
+  PKV_ERR_ALIGN = -4,        /* a pointer is not aligned as the layout requires */
+  PKV_ERR_WORKSPACE = -5,    /* workspace missing or smaller than required */
+  PKV_ERR_CUDA = -6,         /* a CUDA runtime/driver call failed */
+  PKV_ERR_DEVICE = -7        /* reserved: a kernel recorded a device-side error */
+};
+
+/* Device-side error codes (pkv_get_device_error). */
+enum {
+  PKV_DEV_OK = 0,
+  PKV_DEV_BAD_BLOCK_ID = 1,  /* a block table entry outside [0, num_blocks) */
+  PKV_DEV_BAD_CONTEXT = 2,   /* a context length outside [1, max_context_len] */
+  PKV_DEV_BAD_SLOT = 3,      /* a slot >= num_blocks * block_size */
+  PKV_DEV_TIMEOUT = 4        /* a pipeline wait gave up (should never happen) */
+};
+
+/* Shape of one paged cache and of the batch that reads it.
+ *   num_seqs            B, sequences in the batch (one query token each)
+ *   num_q_heads         Hq
+ *   num_kv_heads        Hkv; Hq % Hkv == 0; query head h reads kv head
+ *                       h / (Hq / Hkv) (contiguous grouping)
+ *   head_dim            D, one of 64, 128, 256
+ *   block_size          bs, tokens per physical block, one of 16, 32
+ *   num_blocks          NB, physical blocks in the pool
+ *   max_blocks_per_seq  MB, row stride of block_tables
+ *   max_context_len     host-known upper bound on every context_lens[i]
+ *                       (1 <= it <= MB * bs); sizes the split-KV grid
+ *   dtype               pkv_dtype
+ *   split_tokens        tokens per split-KV partition; 0 lets the library
+ *                       choose; otherwise rounded up to a multiple of bs */
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t max_context_len;
+  int32_t dtype;
+  int32_t split_tokens;
+} pkv_shape;
+
+/* How a decode call will run (filled by pkv_decode_plan). */
+typedef struct {
+  int32_t split_tokens;     /* P, tokens per partition (multiple of bs) */
+  int32_t num_splits;       /* S = ceil(max_context_len / P) */
+  int32_t variant;          /* 0 = CUDA-core kernel, 1 = tensor-core (mma) kernel */
+  int32_t warps_per_cta;
+  int32_t stages_per_warp;
+  int32_t grid_ctas;        /* B * Hkv * S */
+  size_t workspace_bytes;   /* 0 when S == 1 */
+} pkv_plan;
+
+/*
+ * KV append (slot scatter).  For every token t in [0, num_tokens) with
+ * s = slot_mapping[t] >= 0, and every kv head h:
+ *     k_cache[s / bs][h][s % bs][:] = k[t][h][:]
+ *     v_cache[s / bs][h][s % bs][:] = v[t][h][:]
+ * A negative slot means "write nothing" (padding).  Bit-exact copy.
+ *
+ *   shape         uses num_kv_heads, head_dim, block_size, num_blocks, dtype
+ *   k, v          [num_tokens, Hkv, D], 16-byte aligned
+ *   slot_mapping  [num_tokens] int32
+ *   k_cache, v_cache  [NB, Hkv, bs, D], 16-byte aligned
+ * Slots >= NB * bs are skipped and set PKV_DEV_BAD_SLOT.  Two tokens with the
+ * same non-negative slot race (undefined which one lands).  num_tokens == 0 is
+ * a no-op.
+ */
+int pkv_kv_cache_append(const pkv_shape* shape, const void* k, const void* v,
+                        const int32_t* slot_mapping, int32_t num_tokens,
+                        void* k_cache, void* v_cache, pkv_stream_t stream);
+
+/*
+ * Paged single-token decode attention.  For every sequence i and query head h,
+ * with g = h / (Hq / Hkv) and L = context_lens[i]:
+ *     k_t = k_cache[block_tables[i][t / bs]][g][t % bs][:],  t in [0, L)
+ *     out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) * v_t
+ * (v_t likewise from v_cache).
+ *
+ *   q, out            [B, Hq, D], 16-byte aligned
+ *   k_cache, v_cache  [NB, Hkv, bs, D], 16-byte aligned
+ *   block_tables      [B, MB] int32; entries past ceil(L / bs) are never read
+ *   context_lens      [B] int32, each in [1, max_context_len]; counts the token
+ *                     appended in this step
+ *   scale             softmax scale (typically 1 / sqrt(D))
+ *   workspace         caller-owned device scratch for split-KV partials, at
+ *                     least pkv_plan.workspace_bytes (may be NULL when that
+ *                     is 0), 16-byte aligned; its contents need no
+ *                     initialisation.  Calls that share a workspace must not
+ *                     overlap on the GPU.
+ * A sequence whose length or block ids are out of range is skipped (its out
+ * rows are left unwritten) and the device error word is set.  B == 0 is a
+ * no-op.
+ */
+int pkv_paged_attn_decode(const pkv_shape* shape, const void* q,
+                          const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables,
+                          const int32_t* context_lens, float scale, void* out,
+                          void* workspace, size_t workspace_bytes,
+                          pkv_stream_t stream);
+
+/* Validate `shape` and report how pkv_paged_attn_decode will run on the
+ * current device (split size, kernel variant, workspace size).  Host only;
+ * reads device attributes once. */
+int pkv_decode_plan(const pkv_shape* shape, pkv_plan* plan);
+
+/* Workspace bytes pkv_paged_attn_decode needs for `shape` (0 if none). */
+int pkv_workspace_bytes(const pkv_shape* shape, size_t* bytes);
+
+/* Read and clear the device-side error word of the current device.
+ * Synchronises `stream`.  *code receives a PKV_DEV_* value (first error since
+ * the last read). */
+int pkv_get_device_error(int32_t* code, pkv_stream_t stream);
+
+/* Human-readable text for a PKV_ERR_* code (static storage). */
+const char* pkv_strerror(int code);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t pkv_launch_count(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,415 @@
+// C-ABI front end of libpkv: argument validation, split-KV planning, TMA
+// descriptor encoding, and the KV append and cross-split reduce launches.
+// The declarations and the contract of every entry point are in include/pkv.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_decode.cuh"
+#include "pkv_geometry.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+__device__ int g_device_error;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// ------------------------------------------------------------------ append
+// KV append scatter (block manager slot write): one warp per (token, kv head)
+// row; the warp copies the K row then the V row with 16-byte vector stores.
+__global__ void __launch_bounds__(256)
+    kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                     const int32_t* __restrict__ slot_mapping, uint4* __restrict__ k_cache,
+                     uint4* __restrict__ v_cache, int T, int Hkv, int bs, int NB,
+                     int chunks_per_row, int* err) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(T) * Hkv) return;
+  const int t = static_cast<int>(row / Hkv);
+  const int h = static_cast<int>(row - static_cast<long long>(t) * Hkv);
+  const int s = slot_mapping[t];
+  if (s < 0) return;
+  if (static_cast<long long>(s) >= static_cast<long long>(NB) * bs) {
+    if (lane == 0 && h == 0) record_error(err, kDevBadSlot);
+    return;
+  }
+  const size_t dst = ((static_cast<size_t>(s / bs) * Hkv + h) * bs + (s % bs)) * chunks_per_row;
+  const size_t src = static_cast<size_t>(row) * chunks_per_row;
+  for (int c = lane; c < 2 * chunks_per_row; c += 32) {
+    if (c < chunks_per_row) {
+      k_cache[dst + c] = k[src + c];
+    } else {
+      const int cc = c - chunks_per_row;
+      v_cache[dst + cc] = v[src + cc];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ reduce
+template <bool BF>
+cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
+  const int rows = a.B * a.Hq;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  switch (D) {
+    case 64:
+      split_reduce_kernel<BF, 64><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.context_lens,
+                                                           a.out, a.B, a.Hq, a.S, a.P, a.max_ctx);
+      break;
+    case 128:
+      split_reduce_kernel<BF, 128><<<grid, 256, 0, stream>>>(
+          a.part_o, a.part_ml, a.context_lens, a.out, a.B, a.Hq, a.S, a.P, a.max_ctx);
+      break;
+    case 256:
+      split_reduce_kernel<BF, 256><<<grid, 256, 0, stream>>>(
+          a.part_o, a.part_ml, a.context_lens, a.out, a.B, a.Hq, a.S, a.P, a.max_ctx);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ devices
+struct DeviceInfo {
+  bool valid = false;
+  int sms = 0;
+  int* err = nullptr;
+};
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+int current_device(DeviceInfo** info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.valid) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return PKV_ERR_CUDA;
+    d.err = static_cast<int*>(p);
+    d.valid = true;
+  }
+  *info = &d;
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------------ TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// The pool [NB, Hkv, bs, D] as a 2-D tensor of NB * Hkv * bs rows of D
+// elements; one box is 64 elements (128 bytes) x bs rows with the 128-byte
+// swizzle, so one [bs, D] tile is D / 64 boxes.
+int encode_cache_map(CUtensorMap* map, const void* base, const pkv_shape& s) {
+  const cuuint64_t rows = static_cast<cuuint64_t>(s.num_blocks) * s.num_kv_heads * s.block_size;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.head_dim), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(s.block_size)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      s.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+struct MapCacheEntry {
+  const void* base = nullptr;
+  pkv_shape shape{};
+  int device = -1;
+  CUtensorMap map{};
+};
+std::mutex g_map_mutex;
+MapCacheEntry g_map_cache[8];
+int g_map_next = 0;
+
+int cache_map(CUtensorMap* out, const void* base, const pkv_shape& s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  for (auto& e : g_map_cache) {
+    if (e.base == base && e.device == dev && e.shape.num_blocks == s.num_blocks &&
+        e.shape.num_kv_heads == s.num_kv_heads && e.shape.block_size == s.block_size &&
+        e.shape.head_dim == s.head_dim && e.shape.dtype == s.dtype) {
+      *out = e.map;
+      return PKV_OK;
+    }
+  }
+  MapCacheEntry& e = g_map_cache[g_map_next];
+  g_map_next = (g_map_next + 1) % 8;
+  int rc = encode_cache_map(&e.map, base, s);
+  if (rc != PKV_OK) {
+    e.base = nullptr;
+    return rc;
+  }
+  e.base = base;
+  e.shape = s;
+  e.device = dev;
+  *out = e.map;
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------------ checks
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cache_shape(const pkv_shape* s) {
+  if (!s) return PKV_ERR_NULL;
+  if (s->num_kv_heads < 1 || s->head_dim < 1 || s->block_size < 1 || s->num_blocks < 1)
+    return PKV_ERR_INVALID;
+  if (s->dtype != PKV_F16 && s->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (s->head_dim != 64 && s->head_dim != 128 && s->head_dim != 256) return PKV_ERR_UNSUPPORTED;
+  if (s->block_size != 16 && s->block_size != 32) return PKV_ERR_UNSUPPORTED;
+  // TMA row coordinates are 32-bit signed
+  if (static_cast<long long>(s->num_blocks) * s->num_kv_heads * s->block_size >= (1ll << 31))
+    return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+int check_decode_shape(const pkv_shape* s) {
+  int rc = check_cache_shape(s);
+  if (rc != PKV_OK) return rc;
+  if (s->num_seqs < 0 || s->num_q_heads < 1 || s->max_blocks_per_seq < 1 ||
+      s->max_context_len < 1 || s->split_tokens < 0)
+    return PKV_ERR_INVALID;
+  if (s->num_q_heads % s->num_kv_heads != 0) return PKV_ERR_INVALID;
+  if (static_cast<long long>(s->max_context_len) >
+      static_cast<long long>(s->max_blocks_per_seq) * s->block_size)
+    return PKV_ERR_INVALID;
+  const int G = s->num_q_heads / s->num_kv_heads;
+  if (G > 8) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
+  const int G = s->num_q_heads / s->num_kv_heads;
+  const int bs = s->block_size;
+  plan->variant = G <= 2 ? 0 : 1;
+  KernelGeometry geo{};
+  decode_geometry(s->head_dim, bs, plan->variant, &geo);
+  plan->warps_per_cta = geo.warps;
+  plan->stages_per_warp = geo.stages;
+  const long long units = static_cast<long long>(s->num_seqs) * s->num_kv_heads;
+  const int maxL = s->max_context_len;
+  const int gran = bs * geo.warps;           // every warp gets the same block count
+  const int cap = kMaxBlocksPerCta * bs;      // ids of one partition fit in shared memory
+  long long P;
+  if (s->split_tokens > 0) {
+    P = (static_cast<long long>(s->split_tokens) + bs - 1) / bs * bs;
+  } else {
+    // Default 512 tokens per partition (bounds the per-CTA tail); shrink it
+    // when the grid would not fill every SM twice over, never below one block
+    // per warp.
+    P = 512;
+    const long long want = 2LL * sms * 2;
+    if (units > 0 && units * ((maxL + P - 1) / P) < want) {
+      const long long S = (want + units - 1) / units;
+      P = (maxL + S - 1) / S;
+      P = (P + gran - 1) / gran * gran;
+    }
+    // At most 1024 partitions per sequence.
+    const long long pmin = (static_cast<long long>(maxL) + 1023) / 1024;
+    if (P < pmin) P = (pmin + gran - 1) / gran * gran;
+  }
+  if (P > cap) P = cap;
+  if (P > maxL) P = (maxL + bs - 1) / bs * bs;
+  if (P < bs) P = bs;
+  plan->split_tokens = static_cast<int32_t>(P);
+  plan->num_splits = static_cast<int32_t>((maxL + P - 1) / P);
+  const long long grid = units * plan->num_splits;
+  if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  plan->grid_ctas = static_cast<int32_t>(grid);
+  plan->workspace_bytes =
+      plan->num_splits > 1
+          ? static_cast<size_t>(s->num_seqs) * s->num_q_heads * plan->num_splits *
+                (static_cast<size_t>(s->head_dim) * 4 + 8)
+          : 0;
+  return PKV_OK;
+}
+
+}  // namespace
+
+bool decode_geometry(int D, int BS, int variant, KernelGeometry* g) {
+  (void)variant;
+  g->warps = geo_warps(D, BS);
+  g->stages = geo_stages(D, BS);
+  g->smem_bytes = geo_smem(D, BS);
+  return true;
+}
+
+int* device_error_word() {
+  DeviceInfo* d = nullptr;
+  return current_device(&d) == PKV_OK ? d->err : nullptr;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_version(void) { return 100; }
+
+extern "C" uint64_t pkv_launch_count(void) { return g_launches.load(); }
+
+extern "C" const char* pkv_strerror(int code) {
+  switch (code) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "a required pointer is NULL";
+    case PKV_ERR_INVALID: return "invalid size (non-positive dimension, Hq % Hkv != 0, or max_context_len > max_blocks_per_seq * block_size)";
+    case PKV_ERR_UNSUPPORTED: return "unsupported head_dim, block_size, group size, dtype or pool size";
+    case PKV_ERR_ALIGN: return "a pointer is not 16-byte (arrays of 16-bit elements) or 4-byte (int32 arrays) aligned";
+    case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than pkv_workspace_bytes";
+    case PKV_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case PKV_ERR_DEVICE: return "a kernel recorded a device-side error";
+    default: return "unknown pkv error code";
+  }
+}
+
+extern "C" int pkv_decode_plan(const pkv_shape* s, pkv_plan* plan) {
+  if (!s || !plan) return PKV_ERR_NULL;
+  int rc = check_decode_shape(s);
+  if (rc != PKV_OK) return rc;
+  DeviceInfo* d = nullptr;
+  rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  return make_plan(s, d->sms, plan);
+}
+
+extern "C" int pkv_workspace_bytes(const pkv_shape* s, size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  pkv_plan plan{};
+  int rc = pkv_decode_plan(s, &plan);
+  if (rc != PKV_OK) return rc;
+  *bytes = plan.workspace_bytes;
+  return PKV_OK;
+}
+
+extern "C" int pkv_kv_cache_append(const pkv_shape* s, const void* k, const void* v,
+                                   const int32_t* slot_mapping, int32_t num_tokens,
+                                   void* k_cache, void* v_cache, pkv_stream_t stream) {
+  int rc = check_cache_shape(s);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0) return PKV_ERR_INVALID;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 4))
+    return PKV_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  const long long rows = static_cast<long long>(num_tokens) * s->num_kv_heads;
+  const long long grid = (rows + 7) / 8;
+  if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  kv_append_kernel<<<static_cast<unsigned>(grid), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, s->num_kv_heads,
+      s->block_size, s->num_blocks, s->head_dim / 8, d->err);
+  g_launches.fetch_add(1);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, float scale, void* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     pkv_stream_t stream) {
+  int rc = check_decode_shape(s);
+  if (rc != PKV_OK) return rc;
+  if (s->num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  pkv_plan plan{};
+  rc = make_plan(s, d->sms, &plan);
+  if (rc != PKV_OK) return rc;
+  if (plan.workspace_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16))
+      return PKV_ERR_WORKSPACE;
+  }
+  rc = get_encoder();
+  if (rc != PKV_OK) return rc;
+  CUtensorMap tk, tv;
+  rc = cache_map(&tk, k_cache, *s);
+  if (rc != PKV_OK) return rc;
+  rc = cache_map(&tv, v_cache, *s);
+  if (rc != PKV_OK) return rc;
+
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = static_cast<uint16_t*>(out);
+  const size_t rows = static_cast<size_t>(s->num_seqs) * s->num_q_heads * plan.num_splits;
+  a.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
+  a.part_ml = plan.workspace_bytes
+                  ? reinterpret_cast<float2*>(static_cast<float*>(workspace) + rows * s->head_dim)
+                  : nullptr;
+  a.err = d->err;
+  a.B = s->num_seqs;
+  a.Hq = s->num_q_heads;
+  a.Hkv = s->num_kv_heads;
+  a.G = s->num_q_heads / s->num_kv_heads;
+  a.MB = s->max_blocks_per_seq;
+  a.NB = s->num_blocks;
+  a.S = plan.num_splits;
+  a.P = plan.split_tokens;
+  a.max_ctx = s->max_context_len;
+  a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf = s->dtype == PKV_BF16;
+  cudaError_t e;
+  if (plan.variant == 0)
+    e = bf ? launch_decode_bf16_simt(a, tk, tv, s->head_dim, s->block_size, st)
+           : launch_decode_f16_simt(a, tk, tv, s->head_dim, s->block_size, st);
+  else
+    e = bf ? launch_decode_bf16_mma(a, tk, tv, s->head_dim, s->block_size, st)
+           : launch_decode_f16_mma(a, tk, tv, s->head_dim, s->block_size, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (plan.num_splits > 1) {
+    e = bf ? launch_reduce<true>(a, s->head_dim, st) : launch_reduce<false>(a, s->head_dim, st);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
+  return PKV_OK;
+}
+
+extern "C" int pkv_get_device_error(int32_t* code, pkv_stream_t stream) {
+  if (!code) return PKV_ERR_NULL;
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, d->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (cudaMemsetAsync(d->err, 0, sizeof(int), st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PKV_ERR_CUDA;
+  *code = host;
+  return PKV_OK;
+}

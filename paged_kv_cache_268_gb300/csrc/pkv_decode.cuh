@@ -1,0 +1,515 @@
+// Paged single-token decode attention kernels for sm_103a.
+//
+// One CTA handles one (sequence, kv head, split) unit: the tokens
+// [split * P, min((split + 1) * P, L)) of one sequence, for every query head of
+// the kv head's group.  The method is the paged attention of the third page
+// ("PagedAttention": fixed-size physical blocks, a block table, indirect
+// addressing) computed FlashAttention-style (third page, "FlashAttention deep
+// integration": tile the KV, keep partial results on chip, one pass over HBM),
+// with the plain definition softmax(q . K^T * scale) . V of the second page,
+// section 3.1.
+//
+// Data path, per warp (each warp owns an independent pipeline):
+//   block-table gather  -> the CTA copies its partition's physical block ids
+//                          into shared memory once (and range-checks them)
+//   stage K/V blocks    -> lane 0 issues TMA tiled loads of whole [bs, D] K and
+//                          V tiles (contiguous 2-8 KB each in the
+//                          [NB, Hkv, bs, D] cache) into a ring of NS stages,
+//                          completing on per-stage mbarriers, 128-byte
+//                          swizzled so that the fragment reads below are
+//                          bank-conflict free
+//   QK + online softmax -> FP32 logits in log2 units, running max m and sum l
+//   PV accumulate       -> FP32 output accumulators rescaled by 2^(m_old-m_new)
+// The warps of a CTA then merge their (m, l, o) in shared memory; the CTA
+// writes the normalised output (one split) or its partial (m, l, o) for the
+// cross-split reduce kernel.
+//
+// Two compute variants share that pipeline:
+//   SIMT (group size 1-2): CUDA cores.  Lane (t8 = lane % 8, quarter = lane / 8)
+//     dots token t8 of an 8-row pass with its quarter of q; two xor-shuffles
+//     finish each dot, three more give the block max.  For PV each lane owns
+//     D / 32 output dims.
+//   MMA (group size 3-8): the group's query heads form the N = 8 side of
+//     mma.sync.m16n8k16 tiles.  S^T[16 tok x 8 heads] = K_tile . Q^T (K via
+//     ldmatrix, Q^T fragments held in registers), P^T is transposed in
+//     registers with movmatrix into the B operand of O^T[16 d x 8 heads] +=
+//     V^T . P^T (V via ldmatrix.trans), so a head's column of S^T, P^T and O^T
+//     always lives in the same thread.
+#pragma once
+
+#include "pkv_geometry.h"
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Byte offset of 16-byte chunk `gc` (0 .. D/8-1) of row `r` in a [BS, D] tile
+// stored as D/64 column boxes of BS rows x 128 bytes with the 128-byte swizzle
+// (chunk c of row r sits at chunk position c ^ (r % 8)).
+template <int BS>
+__device__ __forceinline__ uint32_t tile_off(int r, int gc) {
+  return static_cast<uint32_t>((gc >> 3) * BS * 128 + r * 128 + (((gc & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ SIMT
+template <bool BF, int D, int BS, int GH>
+struct SimtCompute {
+  static constexpr int QPL = D / 4;    // q values per lane (its quarter of D)
+  static constexpr int CPQ = D / 32;   // 16-byte chunks per quarter
+  static constexpr int OPL = D / 32;   // output dims per lane
+  static constexpr int PASSES = BS / 8;
+  static constexpr int NH = GH;        // heads this warp produces
+
+  float q[GH][QPL];
+  float o[GH][OPL];
+  float m[GH], l[GH];
+
+  __device__ __forceinline__ void init(const DecodeArgs& a, int seq, int kvh, int lane) {
+    const int dq = lane >> 3;
+#pragma unroll
+    for (int gh = 0; gh < GH; ++gh) {
+      const uint16_t* qrow = a.q + ((size_t)seq * a.Hq + kvh * GH + gh) * D + dq * QPL;
+#pragma unroll
+      for (int i = 0; i < QPL; i += 8) {
+        uint4 u = *reinterpret_cast<const uint4*>(qrow + i);
+        float2 f0 = unpack2<BF>(u.x), f1 = unpack2<BF>(u.y), f2 = unpack2<BF>(u.z),
+               f3 = unpack2<BF>(u.w);
+        q[gh][i + 0] = f0.x; q[gh][i + 1] = f0.y; q[gh][i + 2] = f1.x; q[gh][i + 3] = f1.y;
+        q[gh][i + 4] = f2.x; q[gh][i + 5] = f2.y; q[gh][i + 6] = f3.x; q[gh][i + 7] = f3.y;
+      }
+#pragma unroll
+      for (int e = 0; e < OPL; ++e) o[gh][e] = 0.f;
+      m[gh] = -INFINITY;
+      l[gh] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float scale_log2,
+                                        int lane) {
+    const int t8 = lane & 7, dq = lane >> 3;
+    float s[PASSES][GH];
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = ps * 8 + t8;
+      float acc[GH];
+#pragma unroll
+      for (int gh = 0; gh < GH; ++gh) acc[gh] = 0.f;
+#pragma unroll
+      for (int i = 0; i < CPQ; ++i) {
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                     : "r"(kt + tile_off<BS>(r, dq * CPQ + i)));
+        const float2 f0 = unpack2<BF>(x0), f1 = unpack2<BF>(x1), f2 = unpack2<BF>(x2),
+                     f3 = unpack2<BF>(x3);
+#pragma unroll
+        for (int gh = 0; gh < GH; ++gh) {
+          const float* qq = &q[gh][i * 8];
+          acc[gh] = fmaf(qq[0], f0.x, acc[gh]); acc[gh] = fmaf(qq[1], f0.y, acc[gh]);
+          acc[gh] = fmaf(qq[2], f1.x, acc[gh]); acc[gh] = fmaf(qq[3], f1.y, acc[gh]);
+          acc[gh] = fmaf(qq[4], f2.x, acc[gh]); acc[gh] = fmaf(qq[5], f2.y, acc[gh]);
+          acc[gh] = fmaf(qq[6], f3.x, acc[gh]); acc[gh] = fmaf(qq[7], f3.y, acc[gh]);
+        }
+      }
+#pragma unroll
+      for (int gh = 0; gh < GH; ++gh) {
+        float v = acc[gh];
+        v += __shfl_xor_sync(kFull, v, 8);
+        v += __shfl_xor_sync(kFull, v, 16);
+        s[ps][gh] = (r < valid) ? v * scale_log2 : -INFINITY;
+      }
+    }
+    float p[PASSES][GH];
+#pragma unroll
+    for (int gh = 0; gh < GH; ++gh) {
+      float mx = s[0][gh];
+#pragma unroll
+      for (int ps = 1; ps < PASSES; ++ps) mx = fmaxf(mx, s[ps][gh]);
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+      const float mn = fmaxf(m[gh], mx);
+      const float alpha = fast_exp2(m[gh] - mn);
+      m[gh] = mn;
+      float ls = 0.f;
+#pragma unroll
+      for (int ps = 0; ps < PASSES; ++ps) {
+        p[ps][gh] = fast_exp2(s[ps][gh] - mn);
+        ls += p[ps][gh];
+      }
+      l[gh] = l[gh] * alpha + ls;
+#pragma unroll
+      for (int e = 0; e < OPL; ++e) o[gh][e] *= alpha;
+    }
+    // PV: lane owns dims [lane * OPL, lane * OPL + OPL)
+    constexpr int BYTES = OPL * 2;                  // 4, 8 or 16 bytes per lane per row
+    const int gc = (lane * BYTES) >> 4;
+    const int within = (lane * BYTES) & 15;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int r = ps * 8 + t;
+        if (r < valid) {
+          const uint32_t addr = vt + tile_off<BS>(r, gc) + within;
+          float vf[OPL];
+          if constexpr (OPL == 2) {
+            uint32_t x0;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x0) : "r"(addr));
+            const float2 f0 = unpack2<BF>(x0);
+            vf[0] = f0.x; vf[1] = f0.y;
+          } else if constexpr (OPL == 4) {
+            uint32_t x0, x1;
+            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
+            const float2 f0 = unpack2<BF>(x0), f1 = unpack2<BF>(x1);
+            vf[0] = f0.x; vf[1] = f0.y; vf[2] = f1.x; vf[3] = f1.y;
+          } else {
+            uint32_t x0, x1, x2, x3;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(addr));
+            const float2 f0 = unpack2<BF>(x0), f1 = unpack2<BF>(x1), f2 = unpack2<BF>(x2),
+                         f3 = unpack2<BF>(x3);
+            vf[0] = f0.x; vf[1] = f0.y; vf[2] = f1.x; vf[3] = f1.y;
+            vf[4] = f2.x; vf[5] = f2.y; vf[6] = f3.x; vf[7] = f3.y;
+          }
+#pragma unroll
+          for (int gh = 0; gh < GH; ++gh) {
+            const float pt = __shfl_sync(kFull, p[ps][gh], t);
+#pragma unroll
+            for (int e = 0; e < OPL; ++e) o[gh][e] = fmaf(pt, vf[e], o[gh][e]);
+          }
+        }
+      }
+    }
+  }
+
+  // Leave each head's (m, l, o) for the CTA merge.
+  __device__ __forceinline__ void publish(float* cm, float* cl, float* co, int lane) {
+#pragma unroll
+    for (int gh = 0; gh < GH; ++gh) {
+      float lt = l[gh];
+      lt += __shfl_xor_sync(kFull, lt, 1);
+      lt += __shfl_xor_sync(kFull, lt, 2);
+      lt += __shfl_xor_sync(kFull, lt, 4);
+      if (lane == 0) { cm[gh] = m[gh]; cl[gh] = lt; }
+#pragma unroll
+      for (int e = 0; e < OPL; ++e) co[gh * D + lane * OPL + e] = o[gh][e];
+    }
+  }
+};
+
+// ------------------------------------------------------------------ MMA
+template <bool BF, int D, int BS>
+struct MmaCompute {
+  static constexpr int KS = D / 16;    // k-steps of QK, d-tiles of PV
+  static constexpr int MT = BS / 16;   // 16-token m-tiles per block
+  static constexpr int NH = 8;         // heads this warp produces (N of the tile)
+
+  uint32_t qf[KS][2];                  // Q^T B-fragments
+  float o[KS][4];                      // O^T accumulators
+  float m[2], l[2];                    // heads 2*(lane%4) + {0, 1}
+
+  __device__ __forceinline__ void init(const DecodeArgs& a, int seq, int kvh, int lane) {
+    const int h = lane >> 2;
+    const int c = 2 * (lane & 3);
+    const bool real = h < a.G;
+    const uint16_t* qrow = a.q + ((size_t)seq * a.Hq + kvh * a.G + (real ? h : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qf[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + c) : 0u;
+      qf[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + c) : 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[ks][e] = 0.f;
+    }
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float scale_log2,
+                                        int lane) {
+    float s[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[mt][e] = 0.f;
+      const int r = mt * 16 + (lane & 15);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(kt + tile_off<BS>(r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+        mma_16816<BF>(s[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+    }
+    // logits in log2 units; rows past the context end are masked
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = mt * 16 + (lane >> 2) + ((e >> 1) << 3);
+        const float x = (tok < valid) ? s[mt][e] * scale_log2 : -INFINITY;
+        s[mt][e] = x;
+        mx[e & 1] = fmaxf(mx[e & 1], x);
+      }
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = mx[j];
+      v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(kFull, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(kFull, v, 16));
+      const float mn = fmaxf(m[j], v);
+      alpha[j] = fast_exp2(m[j] - mn);
+      m[j] = mn;
+      l[j] *= alpha[j];
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pe = fast_exp2(s[mt][e] - m[e & 1]);
+        s[mt][e] = pe;
+        l[e & 1] += pe;
+      }
+#pragma unroll
+    for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[dt][e] *= alpha[e & 1];
+
+    if (valid < BS) {
+      // Rows past the context end carry whatever the block held; P is 0 there,
+      // but 0 * NaN would still poison the MMA, so clear those V rows.
+      constexpr int ROWB = 128;
+      const int nz = (BS - valid) * (D / 64) * (ROWB / 16);  // 16-byte stores
+      for (int i = lane; i < nz; i += 32) {
+        const int per_box = (BS - valid) * (ROWB / 16);
+        const int box = i / per_box, rem = i % per_box;
+        const int r = valid + rem / (ROWB / 16), c = rem % (ROWB / 16);
+        const uint32_t addr = vt + box * BS * ROWB + r * ROWB + c * 16;
+        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0) : "memory");
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const uint32_t b0 = movmatrix_trans(pack2<BF>(s[mt][0], s[mt][1]));
+      const uint32_t b1 = movmatrix_trans(pack2<BF>(s[mt][2], s[mt][3]));
+      const int r = mt * 16 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(vt + tile_off<BS>(r, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+        mma_16816<BF>(o[dt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void publish(float* cm, float* cl, float* co, int lane) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float lt = l[j];
+      lt += __shfl_xor_sync(kFull, lt, 4);
+      lt += __shfl_xor_sync(kFull, lt, 8);
+      lt += __shfl_xor_sync(kFull, lt, 16);
+      if (lane < 4) { cm[2 * lane + j] = m[j]; cl[2 * lane + j] = lt; }
+    }
+#pragma unroll
+    for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = dt * 16 + (lane >> 2) + ((e >> 1) << 3);
+        const int h = 2 * (lane & 3) + (e & 1);
+        co[h * D + d] = o[dt][e];
+      }
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+template <bool BF, int D, int BS, int NW, int NS, class Compute>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_kernel(const __grid_constant__ DecodeArgs a,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV) {
+  constexpr int TILE = BS * D * 2;
+  constexpr int STAGE = 2 * TILE;
+  constexpr int CH = D / 64;
+  constexpr int NH = Compute::NH;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NS * STAGE);
+  int* ids = reinterpret_cast<int*>(bars + NW * NS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int idx = blockIdx.x;
+  const int split = idx % a.S;
+  idx /= a.S;
+  const int kvh = idx % a.Hkv;
+  const int seq = idx / a.Hkv;
+
+  const int L = a.context_lens[seq];
+  if (L < 1 || L > a.max_ctx) {
+    if (threadIdx.x == 0 && split == 0 && kvh == 0) record_error(a.err, kDevBadContext);
+    return;
+  }
+  const int t0 = split * a.P;
+  if (t0 >= L) return;
+  const int t1 = min(t0 + a.P, L);
+  const int j0 = t0 / BS;
+  const int nblk = (t1 - t0 + BS - 1) / BS;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  // Block-table gather for this partition (indirect addressing), range-checked.
+  bool bad = false;
+  for (int k = threadIdx.x; k < nblk; k += NW * 32) {
+    const int p = __ldg(a.block_tables + (size_t)seq * a.MB + j0 + k);
+    bad |= (p < 0) | (p >= a.NB);
+    ids[k] = p;
+  }
+  if (threadIdx.x < NW * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
+  if (threadIdx.x == 0) fence_mbar_init();
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) record_error(a.err, kDevBadBlock);
+    return;
+  }
+
+  const int my_n = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+  const uint32_t wbuf = smem_u32(smem + warp * NS * STAGE);
+  const uint32_t wbar = smem_u32(&bars[warp * NS]);
+
+  auto issue = [&](int k) {
+    const int st = k % NS;
+    const int p = ids[warp + NW * k];
+    const int y = (p * a.Hkv + kvh) * BS;
+    const uint32_t bar = wbar + 8 * st;
+    const uint32_t dk = wbuf + st * STAGE;
+    mbar_arrive_expect_tx(bar, STAGE);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      tma_load_2d(dk + c * BS * 128, &tmK, c * 64, y, bar);
+      tma_load_2d(dk + TILE + c * BS * 128, &tmV, c * 64, y, bar);
+    }
+  };
+  if (lane == 0) {
+    const int pro = my_n < NS ? my_n : NS;
+    for (int k = 0; k < pro; ++k) issue(k);
+  }
+
+  Compute cs;
+  cs.init(a, seq, kvh, lane);
+
+  int k = 0;
+  bool ok = true;
+  for (; k < my_n; ++k) {
+    const int st = k % NS;
+    const bool done = mbar_wait(wbar + 8 * st, (k / NS) & 1);
+    if (!__all_sync(kFull, done)) { ok = false; break; }
+    const int jb = j0 + warp + NW * k;
+    const int valid = min(BS, L - jb * BS);
+    const uint32_t kt = wbuf + st * STAGE;
+    cs.block(kt, kt + TILE, valid, a.scale_log2, lane);
+    __syncwarp();
+    if (lane == 0 && k + NS < my_n) {
+      fence_proxy_async_smem();
+      issue(k + NS);
+    }
+  }
+  if (!ok) {
+    // Give every load still in flight a bounded chance to land before the CTA
+    // releases its shared memory, then report.
+    const int hi = min(k + NS, my_n);
+    for (int kk = k; kk < hi; ++kk) mbar_wait(wbar + 8 * (kk % NS), (kk / NS) & 1, 100000000ull);
+    if (lane == 0) record_error(a.err, kDevTimeout);
+  }
+
+  // Merge the warps' (m, l, o) through shared memory (the stage ring is free:
+  // every issued load has been consumed).
+  __syncthreads();
+  float* cm = reinterpret_cast<float*>(smem);
+  float* cl = cm + NW * NH;
+  float* co = cl + NW * NH;
+  cs.publish(cm + warp * NH, cl + warp * NH, co + warp * NH * D, lane);
+  __syncthreads();
+
+  const int nh = (NH == 8) ? a.G : NH;
+  const bool single = (L + a.P - 1) / a.P == 1;
+  for (int i = threadIdx.x; i < nh * D; i += NW * 32) {
+    const int h = i / D, d = i - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, cm[w * NH + h]);
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = fast_exp2(cm[w * NH + h] - M);
+      acc = fmaf(f, co[(w * NH + h) * D + d], acc);
+      lsum = fmaf(f, cl[w * NH + h], lsum);
+    }
+    const size_t row = (size_t)seq * a.Hq + kvh * a.G + h;
+    if (single) {
+      a.out[row * D + d] = to_elem<BF>(acc / lsum);
+    } else {
+      const size_t pr = row * a.S + split;
+      a.part_o[pr * D + d] = acc;
+      if (d == 0) a.part_ml[pr] = make_float2(M, lsum);
+    }
+  }
+}
+
+// Cross-split reduce: one warp per (sequence, query head) with more than one
+// split.  M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
+// summed in split order (deterministic).
+template <bool BF, int D>
+__global__ void __launch_bounds__(256)
+    split_reduce_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                        const int32_t* __restrict__ context_lens, uint16_t* __restrict__ out,
+                        int B, int Hq, int S, int P, int max_ctx) {
+  constexpr int OPL = D / 32;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= B * Hq) return;
+  const int seq = gw / Hq;
+  const int L = context_lens[seq];
+  if (L < 1 || L > max_ctx) return;
+  const int n = (L + P - 1) / P;
+  if (n <= 1) return;
+  const float2* ml = part_ml + (size_t)gw * S;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, ml[s].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  float lsum = 0.f;
+  for (int s = lane; s < n; s += 32) lsum = fmaf(fast_exp2(ml[s].x - M), ml[s].y, lsum);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+  float acc[OPL];
+#pragma unroll
+  for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
+  const float* po = part_o + (size_t)gw * S * D + lane * OPL;
+  for (int s = 0; s < n; ++s) {
+    const float w = fast_exp2(ml[s].x - M);
+    if constexpr (OPL == 2) {
+      const float2 v = *reinterpret_cast<const float2*>(po + (size_t)s * D);
+      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < OPL; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(po + (size_t)s * D + e);
+        acc[e] = fmaf(w, v.x, acc[e]); acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        acc[e + 2] = fmaf(w, v.z, acc[e + 2]); acc[e + 3] = fmaf(w, v.w, acc[e + 3]);
+      }
+    }
+  }
+  uint16_t* orow = out + (size_t)gw * D + lane * OPL;
+#pragma unroll
+  for (int e = 0; e < OPL; ++e) orow[e] = to_elem<BF>(acc[e] / lsum);
+}
+
+}  // namespace pkv

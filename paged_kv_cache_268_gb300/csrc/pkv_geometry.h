@@ -1,0 +1,32 @@
+// Launch geometry of the decode kernels, shared by the host planner and the
+// kernel instantiations so that both agree on shared-memory sizes.
+#pragma once
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// One pipeline stage holds a K tile and a V tile of [block_size, head_dim]
+// 16-bit elements.
+constexpr int stage_bytes(int D, int BS) { return 2 * BS * D * 2; }
+
+// Warps per CTA: four for stages up to 8 KB, fewer for larger tiles, so that a
+// CTA keeps roughly 96 KB of KV in flight and two CTAs fit on one SM.
+constexpr int geo_warps(int D, int BS) {
+  return stage_bytes(D, BS) <= 8192 ? 4 : (stage_bytes(D, BS) <= 16384 ? 2 : 1);
+}
+
+constexpr int geo_stages(int D, int BS) {
+  return (98304 / (geo_warps(D, BS) * stage_bytes(D, BS))) < 2
+             ? 2
+             : 98304 / (geo_warps(D, BS) * stage_bytes(D, BS));
+}
+
+// Stage ring + one mbarrier per stage + the partition's block ids + 1 KB of
+// slack for aligning the ring to the 1024-byte swizzle atom.
+constexpr int geo_smem(int D, int BS) {
+  return geo_warps(D, BS) * geo_stages(D, BS) * stage_bytes(D, BS) +
+         geo_warps(D, BS) * geo_stages(D, BS) * 8 + kMaxBlocksPerCta * 4 + 1024;
+}
+
+}  // namespace pkv

@@ -1,0 +1,57 @@
+// Internal interface between the C-ABI front end (pkv_api.cu) and the decode
+// kernel translation units (pkv_decode_inst.cu, compiled once per element
+// type and kernel variant).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Device error word codes (mirror PKV_DEV_* in include/pkv.h).
+enum : int { kDevBadBlock = 1, kDevBadContext = 2, kDevBadSlot = 3, kDevTimeout = 4 };
+
+// Largest number of KV blocks one CTA's partition may span.
+constexpr int kMaxBlocksPerCta = 256;
+
+struct DecodeArgs {
+  const uint16_t* q;            // [B, Hq, D]
+  const int32_t* block_tables;  // [B, MB]
+  const int32_t* context_lens;  // [B]
+  uint16_t* out;                // [B, Hq, D]
+  float* part_o;                // [B, Hq, S, D] un-normalised partial outputs
+  float2* part_ml;              // [B, Hq, S]   (running max in log2 units, sum)
+  int* err;                     // device error word
+  int B, Hq, Hkv, G, MB, NB;
+  int S;                        // splits per sequence (grid extent)
+  int P;                        // tokens per split, multiple of the block size
+  int max_ctx;                  // upper bound on every context length
+  float scale_log2;             // softmax scale * log2(e)
+};
+
+// Per-(head_dim, block_size, variant) launch geometry.
+struct KernelGeometry {
+  int warps;        // warps per CTA, each with its own KV pipeline
+  int stages;       // pipeline stages per warp (one K tile + one V tile each)
+  int smem_bytes;   // dynamic shared memory per CTA
+};
+
+// Variant: 0 = CUDA-core kernel (group size 1 or 2), 1 = tensor-core kernel
+// (group size 3..8).
+bool decode_geometry(int head_dim, int block_size, int variant, KernelGeometry* g);
+
+// Launch the decode grid (B * Hkv * S CTAs).  Returns cudaErrorInvalidValue
+// for an unbuilt combination.
+cudaError_t launch_decode_f16_simt(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
+                                   int head_dim, int block_size, cudaStream_t);
+cudaError_t launch_decode_bf16_simt(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
+                                    int head_dim, int block_size, cudaStream_t);
+cudaError_t launch_decode_f16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
+                                  int head_dim, int block_size, cudaStream_t);
+cudaError_t launch_decode_bf16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
+                                   int head_dim, int block_size, cudaStream_t);
+
+int* device_error_word();  // device address of the error word (current device)
+
+}  // namespace pkv

@@ -258,6 +258,10 @@ def make(spec: WorkloadSpec | str, seed: int = 0, device: str | torch.device = "
                     k_cache, v_cache)
 
 
-def bits(t: torch.Tensor) -> np.ndarray:
-    """Host copy of a 16-bit tensor as its raw element patterns (uint16)."""
+def bits(t) -> np.ndarray:
+    """Host copy of a 16-bit tensor as its raw element patterns (uint16);
+    uint16 numpy arrays pass through unchanged."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint16
+        return t
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

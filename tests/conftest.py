@@ -16,3 +16,15 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def pkv():
+    """The built CUDA library's binding (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_268_gb300 import _binding, build
+    build.build()
+    _binding.load_library()
+    return _binding

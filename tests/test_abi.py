@@ -1,0 +1,93 @@
+"""The C-ABI library loads, exports every symbol include/pkv.h declares, and
+rejects bad arguments on the host (CPU only: no call here reaches a GPU)."""
+import ctypes
+
+import pytest
+
+from paged_kv_cache_268_gb300 import _binding as B
+from paged_kv_cache_268_gb300 import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = B.header_functions()
+    assert {"pkv_kv_cache_append", "pkv_paged_attn_decode", "pkv_workspace_bytes",
+            "pkv_decode_plan", "pkv_get_device_error", "pkv_strerror",
+            "pkv_launch_count", "pkv_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_and_version(lib):
+    assert lib.pkv_version() >= 100
+    for code in range(0, -8, -1):
+        assert lib.pkv_strerror(code)
+    assert b"unknown" in lib.pkv_strerror(-99)
+    assert lib.pkv_launch_count() == 0
+
+
+def _shape(**kw):
+    base = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                num_blocks=64, max_blocks_per_seq=8, max_context_len=100, dtype=0)
+    base.update(kw)
+    return B.make_shape(**base)
+
+
+FAKE = 0x10000  # 16-byte aligned non-null address; never dereferenced on the host
+
+
+def _decode(lib, shape, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE, ws=None, wsb=0):
+    return lib.pkv_paged_attn_decode(ctypes.byref(shape) if shape is not None else None,
+                                     q, kc, vc, bt, cl, 0.1, out, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_q_heads=6, num_kv_heads=4), -2),          # Hq % Hkv != 0
+    (dict(num_kv_heads=0), -2),
+    (dict(num_seqs=-1), -2),
+    (dict(max_context_len=0), -2),
+    (dict(max_context_len=129), -2),                     # > MB * bs
+    (dict(head_dim=96), -3),
+    (dict(block_size=8), -3),
+    (dict(dtype=5), -3),
+    (dict(num_q_heads=32, num_kv_heads=2), -3),          # group of 16 not built
+    (dict(num_blocks=1 << 24, num_kv_heads=8, num_q_heads=8), -3),  # rows overflow int32
+])
+def test_decode_rejects_bad_shapes(lib, kw, code):
+    assert _decode(lib, _shape(**kw)) == code
+
+
+def test_decode_null_and_alignment(lib):
+    assert _decode(lib, None) == -1
+    assert _decode(lib, _shape(), q=None) == -1
+    assert _decode(lib, _shape(), out=None) == -1
+    assert _decode(lib, _shape(), q=FAKE + 2) == -4
+    assert _decode(lib, _shape(), bt=FAKE + 2) == -4
+    # an empty batch is a no-op that never touches the GPU
+    assert _decode(lib, _shape(num_seqs=0), q=None) == 0
+
+
+def test_append_rejects_bad_args(lib):
+    s = _shape()
+    f = lib.pkv_kv_cache_append
+    assert f(None, FAKE, FAKE, FAKE, 1, FAKE, FAKE, None) == -1
+    assert f(ctypes.byref(s), None, FAKE, FAKE, 1, FAKE, FAKE, None) == -1
+    assert f(ctypes.byref(s), FAKE, FAKE, FAKE, -1, FAKE, FAKE, None) == -2
+    assert f(ctypes.byref(s), FAKE + 8, FAKE, FAKE, 1, FAKE, FAKE, None) == -4
+    assert f(ctypes.byref(_shape(head_dim=80)), FAKE, FAKE, FAKE, 1, FAKE, FAKE, None) == -3
+    assert f(ctypes.byref(s), None, None, None, 0, None, None, None) == 0   # no tokens: no-op
+    assert lib.pkv_launch_count() == 0
+
+
+def test_plan_rejects_before_device(lib):
+    p = B.Plan()
+    assert lib.pkv_decode_plan(None, ctypes.byref(p)) == -1
+    assert lib.pkv_decode_plan(ctypes.byref(_shape(head_dim=48)), ctypes.byref(p)) == -3
+    n = ctypes.c_size_t(0)
+    assert lib.pkv_workspace_bytes(ctypes.byref(_shape()), None) == -1
+    assert lib.pkv_workspace_bytes(ctypes.byref(_shape(num_kv_heads=3)), ctypes.byref(n)) == -2

@@ -1,0 +1,145 @@
+"""GPU parity of paged_attn_decode against the CPU oracle (through the C ABI).
+
+Tolerance: |gpu - ref| <= 2e-3 + 1e-2 |ref| elementwise, the bound stated for
+fp16/bf16 output with fp32 accumulation."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_268_gb300 import workloads as W
+from parity import assert_close, device_inputs, gpu_decode, oracle_decode, widen_out
+
+pytestmark = pytest.mark.gpu
+
+# Oracle-sized versions of the five workloads: same heads, head_dim, block
+# size, dtype and structure; fewer, shorter sequences spanning several tiles,
+# several splits and a ragged last block.
+SMALL = {
+    "tiny_mha": W.WORKLOADS["tiny_mha"],
+    "llama7b_mha": W.scaled(W.WORKLOADS["llama7b_mha"], 6, 1300),
+    "llama3_8b_gqa": W.scaled(W.WORKLOADS["llama3_8b_gqa"], 8, 1500, min_len=16),
+    "long_ctx_gqa": W.scaled(W.WORKLOADS["long_ctx_gqa"], 2, 2600, lens="fixed"),
+    "cont_batch": W.scaled(W.WORKLOADS["cont_batch"], 16, 700),
+}
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("name", W.ORDER)
+def test_small_workloads(pkv, name, seed):
+    w = W.make(SMALL[name], seed=seed)
+    assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), f"{name}/{seed}")
+
+
+@pytest.mark.parametrize("split", [16, 64, 256, 512, 1 << 20])
+def test_split_count_invariance(pkv, split):
+    """Every split size gives the oracle's answer within tolerance."""
+    for name in ("llama7b_mha", "long_ctx_gqa"):
+        w = W.make(SMALL[name], seed=5)
+        assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), oracle_decode(w),
+                     f"{name}/split={split}")
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 6, 8])
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 16), (128, 32), (256, 16), (64, 32), (256, 32)])
+def test_shape_sweep(pkv, dtype, G, D, bs):
+    Hkv = 2
+    spec = W.WorkloadSpec("sweep", 5, G * Hkv, Hkv, D, bs, dtype, 0, 0, "uniform", (1, 1))
+    lens = np.array([1, bs - 1, bs, bs + 1, 3 * bs + 5], dtype=np.int32)
+    spec = W.scaled(spec, 5, int(lens.max()))
+    w = W.make(spec, seed=G * 1000 + D + bs, lens=lens)
+    for split in (0, bs):
+        assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), oracle_decode(w),
+                     f"G={G} D={D} bs={bs} split={split}")
+
+
+def test_edge_lengths(pkv):
+    """ctx = 1, multiples of the block size and one either side, long tails."""
+    lens = np.array([1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025], dtype=np.int32)
+    for base in ("llama7b_mha", "llama3_8b_gqa"):
+        spec = W.scaled(W.WORKLOADS[base], len(lens), int(lens.max()))
+        w = W.make(spec, seed=11, lens=lens)
+        assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), base)
+
+
+def test_all_context_one_returns_v(pkv):
+    spec = W.scaled(W.WORKLOADS["llama3_8b_gqa"], 4, 1)
+    w = W.make(spec, seed=2, lens=np.ones(4, dtype=np.int32))
+    out = widen_out(gpu_decode(pkv, w))
+    G = spec.group
+    for i in range(4):
+        p = w.block_tables[i, 0]
+        v0 = w.v_cache[p, :, 0, :].double().cpu().numpy()
+        for h in range(spec.num_q_heads):
+            assert np.array_equal(out[i, h], v0[h // G])
+
+
+def test_deterministic_and_shared_rows_identical(pkv):
+    """Repeated calls are bit-identical; sequences with identical q, table and
+    length give bit-identical rows (the shared-prefix sanity check)."""
+    w = W.make(SMALL["cont_batch"], seed=3)
+    d = device_inputs(w)
+    d["q"][1] = d["q"][0]
+    d["block_tables"][1] = d["block_tables"][0]
+    d["context_lens"][1] = d["context_lens"][0]
+    a = gpu_decode(pkv, w, d)
+    b = gpu_decode(pkv, w, d)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a[0].view(torch.int16), a[1].view(torch.int16))
+
+
+def test_bad_block_id_sets_device_error(pkv):
+    """An out-of-range table entry is caught by the kernel's own range check:
+    the unit is skipped and the error word reads PKV_DEV_BAD_BLOCK_ID."""
+    w = W.make(SMALL["llama3_8b_gqa"], seed=0)
+    d = device_inputs(w)
+    d["block_tables"][2, 0] = w.spec.num_blocks + 7
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], w.scale, max_context_len=w.max_context_len)
+    assert pkv.get_device_error() == 1
+    assert pkv.get_device_error() == 0          # read clears it
+    d["block_tables"][2, 0] = -3
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], w.scale, max_context_len=w.max_context_len)
+    assert pkv.get_device_error() == 1
+
+
+def test_bad_context_len_sets_device_error(pkv):
+    w = W.make(SMALL["llama7b_mha"], seed=0)
+    d = device_inputs(w)
+    d["context_lens"][1] = 0
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], w.scale, max_context_len=w.max_context_len)
+    assert pkv.get_device_error() == 2
+    d["context_lens"][1] = w.max_context_len + 1
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], w.scale, max_context_len=w.max_context_len)
+    assert pkv.get_device_error() == 2
+
+
+def _sample_rows(w: W.Workload, n: int, rng) -> np.ndarray:
+    B, Hq = w.spec.num_seqs, w.spec.num_q_heads
+    n = min(n, B * Hq)
+    longest = int(np.argmax(w.context_lens))
+    shortest = int(np.argmin(w.context_lens))
+    rows = {(longest, 0), (longest, Hq - 1), (shortest, Hq // 2), (B - 1, Hq - 1)}
+    while len(rows) < n:
+        rows.add((int(rng.integers(B)), int(rng.integers(Hq))))
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_full_size_sampled(pkv, name):
+    """Full-size workloads in the benchmark's launch configuration; the oracle
+    recomputes a sample of (sequence, head) rows one by one."""
+    w = W.make(name, seed=0, device="cuda")
+    d = device_inputs(w)
+    out = widen_out(gpu_decode(pkv, w, d))
+    rows = _sample_rows(w, 48, np.random.default_rng(0))
+    ref = oracle.decode_rows(rows, W.bits(w.q), W.bits(w.k_cache), W.bits(w.v_cache),
+                             w.block_tables, w.context_lens, w.scale, w.spec.dtype)
+    assert_close(out[rows[:, 0], rows[:, 1]], ref, name)
+    assert np.all(np.isfinite(out))
