@@ -153,6 +153,28 @@ int pkv_paged_attn_decode(const pkv_shape* shape, const void* q,
                           void* workspace, size_t workspace_bytes,
                           pkv_stream_t stream);
 
+/*
+ * pkv_paged_attn_decode for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this call; it exists for callers that own all
+ * device memory themselves (an engine that reserved HBM for its KV block pool
+ * and offers no allocator) or cannot afford cudaMalloc on their decode path.
+ * Same arguments, layouts and results as pkv_paged_attn_decode, minus the
+ * workspace: the split-KV partials go to a fixed 64 MiB array inside the
+ * library (held on every GPU that loads the library until the process exits).
+ *  - Returns PKV_ERR_WORKSPACE, enqueuing nothing, when the call's partials
+ *    (pkv_plan.workspace_bytes) exceed 64 MiB; raise split_tokens to fit.
+ *  - The first call on a device looks up the array's address on that device;
+ *    make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (nothing in it needs clearing): calls that overlap on the GPU
+ *    race.  Never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+int pkv_paged_attn_decode_noalloc(const pkv_shape* shape, const void* q,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables,
+                                  const int32_t* context_lens, float scale,
+                                  void* out, pkv_stream_t stream);
+
 /* Validate `shape` and report how pkv_paged_attn_decode will run on the
  * current device (split size, kernel variant, workspace size).  Host only;
  * reads device attributes once. */

@@ -1,0 +1,69 @@
+"""pkv_paged_attn_decode_noalloc, the decode entry point for callers that
+cannot allocate device memory (an engine that owns all of HBM through its own
+KV block pool, or a decode path where cudaMalloc's device-wide sync is not
+acceptable).  It keeps the split-KV partials in a fixed array inside the
+library, so the caller passes only inputs and outputs.
+
+Called through the C ABI and checked against the regular entry point (which
+takes a caller-allocated workspace) within the parity tolerance, on two calls
+in a row so that the second call runs over the first call's leftover scratch.
+This file is collected last on purpose."""
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+import torch
+
+from paged_kv_cache_268_gb300 import workloads as W
+from parity import assert_close, device_inputs, widen_out
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(lib):
+    f = lib.pkv_paged_attn_decode_noalloc
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return f
+
+
+def _call_noalloc(pkv, d, out, scale, max_context_len, split_tokens=0):
+    shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], max_context_len,
+                             split_tokens)
+    f = _noalloc(pkv.load_library())
+    return f(ctypes.addressof(shape), d["q"].data_ptr(), d["k_cache"].data_ptr(),
+             d["v_cache"].data_ptr(), d["block_tables"].data_ptr(),
+             d["context_lens"].data_ptr(), scale, out.data_ptr(),
+             torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_matches_workspace_entry_point(pkv):
+    cases = [W.make(W.scaled(W.WORKLOADS["long_ctx_gqa"], 2, 3000, lens="fixed"), seed=1),
+             W.make(W.scaled(W.WORKLOADS["llama7b_mha"], 6, 1300), seed=2)]
+    for w in cases:                       # two calls in a row, different batches
+        d = device_inputs(w)
+        shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len)
+        assert pkv.decode_plan(shape).num_splits > 1      # the scratch is really used
+        out = torch.full_like(d["q"], float("nan"))
+        assert _call_noalloc(pkv, d, out, w.scale, w.max_context_len) == 0
+        ref = pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                    d["context_lens"], w.scale,
+                                    max_context_len=w.max_context_len)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert_close(widen_out(out), widen_out(ref), f"noalloc vs workspace, {w.spec.name}")
+
+
+def test_noalloc_rejects_oversized_partials(pkv):
+    # 256 sequences x 64 heads x 2048 partitions of 16 tokens: far beyond
+    # 64 MiB of partials, rejected on the host before anything is enqueued
+    spec = W.WorkloadSpec("big", 256, 64, 8, 128, 16, W.BF16, 300, 2048, "fixed", (1,) * 256)
+    w = W.make(spec, seed=0)
+    d = device_inputs(w)
+    out = torch.empty_like(d["q"])
+    shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], 2048 * 16, 16)
+    assert pkv.decode_plan(shape).workspace_bytes > 64 << 20
+    n0 = pkv.launch_count()
+    assert _call_noalloc(pkv, d, out, w.scale, 2048 * 16, split_tokens=16) == -5
+    assert pkv.launch_count() == n0
