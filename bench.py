@@ -418,6 +418,8 @@ def run_pkv(args):
                    "pool_blocks": spec.num_blocks, "context_lens": f"{spec.lens}{tuple(spec.len_args)}",
                    "sum_context_len": int(w.context_lens.sum()), "seed": args.seed,
                    "step": "kv_cache_append(1 token/seq) + paged_attn_decode",
+                   "schedule": "persistent" if plan.schedule == 1 else "partitions",
+                   "grid_ctas": plan.grid_ctas,
                    "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
                    "kernel_variant": "mma" if plan.variant else "simt",
                    "l2": f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB L2)",
@@ -428,7 +430,7 @@ def run_pkv(args):
         "decode_ms_median": statistics.median(decode_ms),
         "decode_ms_p90": float(np.percentile(decode_ms, 90)),
         "append_us_median": 1e3 * statistics.median(append_ms),
-        "roofline": {"bound": "hbm", "kernel": "paged_attn_decode (decode + split reduce)",
+        "roofline": {"bound": "hbm", "kernel": "paged_attn_decode (decode + merge kernels)",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes},

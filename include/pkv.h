@@ -94,15 +94,23 @@ typedef struct {
   int32_t split_tokens;
 } pkv_shape;
 
-/* How a decode call will run (filled by pkv_decode_plan). */
+/* How a decode call will run (filled by pkv_decode_plan).
+ *   schedule 1 (default, split_tokens == 0 and num_seqs <= 2048): persistent
+ *     kernel, grid_ctas = 2 per SM; every warp streams an equal share of all
+ *     KV blocks of the batch, and a merge kernel combines the units a warp
+ *     boundary cut.
+ *   schedule 0 (split_tokens > 0, or larger batches): one CTA per (sequence,
+ *     kv head, partition of split_tokens tokens), grid_ctas = B * Hkv * S,
+ *     then a cross-partition reduce kernel when S > 1. */
 typedef struct {
-  int32_t split_tokens;     /* P, tokens per partition (multiple of bs) */
-  int32_t num_splits;       /* S = ceil(max_context_len / P) */
+  int32_t schedule;
+  int32_t split_tokens;     /* P, tokens per partition (schedule 0; else 0) */
+  int32_t num_splits;       /* S = ceil(max_context_len / P) (schedule 0; else 0) */
   int32_t variant;          /* 0 = CUDA-core kernel, 1 = tensor-core (mma) kernel */
   int32_t warps_per_cta;
   int32_t stages_per_warp;
-  int32_t grid_ctas;        /* B * Hkv * S */
-  size_t workspace_bytes;   /* 0 when S == 1 */
+  int32_t grid_ctas;
+  size_t workspace_bytes;   /* 0 when no partials are needed */
 } pkv_plan;
 
 /*

@@ -36,14 +36,16 @@ class Shape(ctypes.Structure):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("split_tokens", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+    _fields_ = [("schedule", ctypes.c_int32), ("split_tokens", ctypes.c_int32),
+                ("num_splits", ctypes.c_int32),
                 ("variant", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
                 ("stages_per_warp", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t)]
 
 
 def library_path() -> str:
-    return _build.LIB
+    """libpkv.so to load: $PKV_LIBRARY if set, else the in-tree build."""
+    return os.environ.get("PKV_LIBRARY") or _build.LIB
 
 
 def load_library(path: str | None = None):

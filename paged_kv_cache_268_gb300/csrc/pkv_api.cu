@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -73,6 +74,56 @@ cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <bool BF>
+cudaError_t launch_merge(const DecodeArgs& a, int D, cudaStream_t stream) {
+  const int rows = a.B * a.Hq;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  switch (D) {
+    case 64:
+      persistent_merge_kernel<BF, 64><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.hdr, a.out,
+                                                               a.B, a.Hq, a.Hkv);
+      break;
+    case 128:
+      persistent_merge_kernel<BF, 128><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.hdr,
+                                                                a.out, a.B, a.Hq, a.Hkv);
+      break;
+    case 256:
+      persistent_merge_kernel<BF, 256><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.hdr,
+                                                                a.out, a.B, a.Hq, a.Hkv);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// Persistent schedule: phase-1 CTAs (two per SM, resident from the start) and
+// phase-2 CTAs (dispatched as SMs free up).  Workspace: header (four int64
+// then cum[0..B]), then the (max, sum) pairs and the outputs of two partial
+// slots per warp of the grid.
+constexpr int kPersistCtasPerSm = 2;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t persist_hdr_bytes(int B) { return round_up((9 + static_cast<size_t>(B)) * 4, 256); }
+
+// Tuning overrides, read once: share of the blocks streamed by phase 1 (per
+// mille, default 750) and phase-2 CTAs per SM (default 4).
+int env_int(const char* name, int dflt, int lo, int hi) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const long x = strtol(v, nullptr, 10);
+  return x < lo ? lo : (x > hi ? hi : static_cast<int>(x));
+}
+int phase1_per_mille() {
+  static const int v = env_int("PKV_PHASE1_PERMILLE", 750, 0, 1000);
+  return v;
+}
+int phase2_ctas_per_sm() {
+  static const int v = env_int("PKV_PHASE2_CTAS_PER_SM", 4, 0, 64);
+  return v;
 }
 
 // ------------------------------------------------------------------ devices
@@ -210,6 +261,23 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   plan->warps_per_cta = geo.warps;
   plan->stages_per_warp = geo.stages;
   const long long units = static_cast<long long>(s->num_seqs) * s->num_kv_heads;
+  const bool persist_ok =
+      s->num_seqs <= kPersistMaxSeqs &&
+      static_cast<long long>(s->num_seqs) * s->max_blocks_per_seq * s->num_kv_heads < (1ll << 31);
+  if (s->split_tokens == 0 && persist_ok) {
+    plan->schedule = 1;
+    plan->split_tokens = 0;
+    plan->num_splits = 0;
+    const int f = phase1_per_mille();
+    const int g2 = f == 1000 ? 0 : sms * phase2_ctas_per_sm();
+    plan->grid_ctas = sms * kPersistCtasPerSm + (g2 > 0 ? g2 : 0);
+    if (f < 1000 && g2 == 0) plan->grid_ctas = sms * kPersistCtasPerSm;
+    const size_t W = static_cast<size_t>(plan->grid_ctas) * geo.warps;
+    plan->workspace_bytes = persist_hdr_bytes(s->num_seqs) + 2 * W * G * 8 +
+                            2 * W * G * static_cast<size_t>(s->head_dim) * 4;
+    return PKV_OK;
+  }
+  plan->schedule = 0;
   const int maxL = s->max_context_len;
   const int gran = bs * geo.warps;           // every warp gets the same block count
   const int cap = kMaxBlocksPerCta * bs;      // ids of one partition fit in shared memory
@@ -363,36 +431,52 @@ extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const vo
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = static_cast<uint16_t*>(out);
-  const size_t rows = static_cast<size_t>(s->num_seqs) * s->num_q_heads * plan.num_splits;
-  a.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
-  a.part_ml = plan.workspace_bytes
-                  ? reinterpret_cast<float2*>(static_cast<float*>(workspace) + rows * s->head_dim)
-                  : nullptr;
+  const int G = s->num_q_heads / s->num_kv_heads;
+  if (plan.schedule == 1) {
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const size_t W = static_cast<size_t>(plan.grid_ctas) * plan.warps_per_cta;
+    a.hdr = reinterpret_cast<int*>(w);
+    a.part_ml = reinterpret_cast<float2*>(w + persist_hdr_bytes(s->num_seqs));
+    a.part_o = reinterpret_cast<float*>(a.part_ml + 2 * W * G);
+  } else {
+    const size_t rows = static_cast<size_t>(s->num_seqs) * s->num_q_heads * plan.num_splits;
+    a.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
+    a.part_ml = plan.workspace_bytes ? reinterpret_cast<float2*>(static_cast<float*>(workspace) +
+                                                                 rows * s->head_dim)
+                                     : nullptr;
+  }
   a.err = d->err;
   a.B = s->num_seqs;
   a.Hq = s->num_q_heads;
   a.Hkv = s->num_kv_heads;
-  a.G = s->num_q_heads / s->num_kv_heads;
+  a.G = G;
   a.MB = s->max_blocks_per_seq;
   a.NB = s->num_blocks;
   a.S = plan.num_splits;
   a.P = plan.split_tokens;
   a.max_ctx = s->max_context_len;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  a.g1 = d->sms * kPersistCtasPerSm;
+  a.f_per_mille = plan.grid_ctas > a.g1 ? phase1_per_mille() : 1000;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = s->dtype == PKV_BF16;
+  const int D = s->head_dim, BS = s->block_size, sc = plan.schedule, grid = plan.grid_ctas;
   cudaError_t e;
   if (plan.variant == 0)
-    e = bf ? launch_decode_bf16_simt(a, tk, tv, s->head_dim, s->block_size, st)
-           : launch_decode_f16_simt(a, tk, tv, s->head_dim, s->block_size, st);
+    e = bf ? launch_decode_bf16_simt(a, tk, tv, D, BS, sc, grid, st)
+           : launch_decode_f16_simt(a, tk, tv, D, BS, sc, grid, st);
   else
-    e = bf ? launch_decode_bf16_mma(a, tk, tv, s->head_dim, s->block_size, st)
-           : launch_decode_f16_mma(a, tk, tv, s->head_dim, s->block_size, st);
+    e = bf ? launch_decode_bf16_mma(a, tk, tv, D, BS, sc, grid, st)
+           : launch_decode_f16_mma(a, tk, tv, D, BS, sc, grid, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   g_launches.fetch_add(1);
-  if (plan.num_splits > 1) {
-    e = bf ? launch_reduce<true>(a, s->head_dim, st) : launch_reduce<false>(a, s->head_dim, st);
+  if (plan.schedule == 1) {
+    e = bf ? launch_merge<true>(a, D, st) : launch_merge<false>(a, D, st);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches.fetch_add(1);
+  } else if (plan.num_splits > 1) {
+    e = bf ? launch_reduce<true>(a, D, st) : launch_reduce<false>(a, D, st);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     g_launches.fetch_add(1);
   }

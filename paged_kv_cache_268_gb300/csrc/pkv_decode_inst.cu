@@ -14,49 +14,70 @@ namespace {
 
 constexpr bool kBF = PKV_INST_BF16 != 0;
 
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <class K>
+cudaError_t configure(K kern, int smem, int* mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 32 && !(*mask & (1 << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    *mask |= 1 << dev;
+  }
+  return cudaSuccess;
+}
+
 template <int D, int BS, class Compute>
 cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                       cudaStream_t stream) {
+                       int schedule, int grid, cudaStream_t stream) {
   constexpr int NW = geo_warps(D, BS);
   constexpr int NS = geo_stages(D, BS);
+  if (schedule == 1) {
+    constexpr int SMEM_MAX = geo_persist_smem(D, BS, kPersistMaxSeqs);
+    static_assert(SMEM_MAX <= 113 * 1024, "two persistent CTAs must fit on one SM");
+    auto kern = paged_decode_persistent<kBF, D, BS, NW, NS, Compute>;
+    static int mask = 0;
+    cudaError_t e = configure(kern, SMEM_MAX, &mask);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NW * 32, geo_persist_smem(D, BS, a.B), stream>>>(a, tk, tv);
+    return cudaGetLastError();
+  }
   constexpr int SMEM = geo_smem(D, BS);
   static_assert(NW * Compute::NH * (D + 2) * 4 <= NW * NS * stage_bytes(D, BS),
                 "merge area must fit in the stage ring");
   auto kern = paged_decode_kernel<kBF, D, BS, NW, NS, Compute>;
-  static int configured_mask = 0;  // one bit per device ordinal (< 32)
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static int mask = 0;
+  cudaError_t e = configure(kern, SMEM, &mask);
   if (e != cudaSuccess) return e;
-  if (dev < 32 && !(configured_mask & (1 << dev))) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    configured_mask |= 1 << dev;
-  }
-  const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * a.S;
-  kern<<<grid, NW * 32, SMEM, stream>>>(a, tk, tv);
+  const unsigned g = static_cast<unsigned>(a.B) * a.Hkv * a.S;
+  kern<<<g, NW * 32, SMEM, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 template <int D, int BS>
 cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                           cudaStream_t stream) {
+                           int schedule, int grid, cudaStream_t stream) {
 #if PKV_INST_MMA
-  if (a.G >= 3 && a.G <= 8) return launch_one<D, BS, MmaCompute<kBF, D, BS>>(a, tk, tv, stream);
+  if (a.G >= 3 && a.G <= 8)
+    return launch_one<D, BS, MmaCompute<kBF, D, BS>>(a, tk, tv, schedule, grid, stream);
 #else
-  if (a.G == 1) return launch_one<D, BS, SimtCompute<kBF, D, BS, 1>>(a, tk, tv, stream);
-  if (a.G == 2) return launch_one<D, BS, SimtCompute<kBF, D, BS, 2>>(a, tk, tv, stream);
+  if (a.G == 1)
+    return launch_one<D, BS, SimtCompute<kBF, D, BS, 1>>(a, tk, tv, schedule, grid, stream);
+  if (a.G == 2)
+    return launch_one<D, BS, SimtCompute<kBF, D, BS, 2>>(a, tk, tv, schedule, grid, stream);
 #endif
   return cudaErrorInvalidValue;
 }
 
 cudaError_t dispatch(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int D,
-                     int BS, cudaStream_t stream) {
-  if (D == 64 && BS == 16) return launch_variant<64, 16>(a, tk, tv, stream);
-  if (D == 64 && BS == 32) return launch_variant<64, 32>(a, tk, tv, stream);
-  if (D == 128 && BS == 16) return launch_variant<128, 16>(a, tk, tv, stream);
-  if (D == 128 && BS == 32) return launch_variant<128, 32>(a, tk, tv, stream);
-  if (D == 256 && BS == 16) return launch_variant<256, 16>(a, tk, tv, stream);
-  if (D == 256 && BS == 32) return launch_variant<256, 32>(a, tk, tv, stream);
+                     int BS, int sc, int grid, cudaStream_t stream) {
+  if (D == 64 && BS == 16) return launch_variant<64, 16>(a, tk, tv, sc, grid, stream);
+  if (D == 64 && BS == 32) return launch_variant<64, 32>(a, tk, tv, sc, grid, stream);
+  if (D == 128 && BS == 16) return launch_variant<128, 16>(a, tk, tv, sc, grid, stream);
+  if (D == 128 && BS == 32) return launch_variant<128, 32>(a, tk, tv, sc, grid, stream);
+  if (D == 256 && BS == 16) return launch_variant<256, 16>(a, tk, tv, sc, grid, stream);
+  if (D == 256 && BS == 32) return launch_variant<256, 32>(a, tk, tv, sc, grid, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -73,8 +94,9 @@ cudaError_t dispatch(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 #endif
 
 cudaError_t PKV_LAUNCH_NAME(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                            int head_dim, int block_size, cudaStream_t stream) {
-  return dispatch(a, tk, tv, head_dim, block_size, stream);
+                            int head_dim, int block_size, int schedule, int grid,
+                            cudaStream_t stream) {
+  return dispatch(a, tk, tv, head_dim, block_size, schedule, grid, stream);
 }
 
 }  // namespace pkv

@@ -29,4 +29,15 @@ constexpr int geo_smem(int D, int BS) {
          geo_warps(D, BS) * geo_stages(D, BS) * 8 + kMaxBlocksPerCta * 4 + 1024;
 }
 
+// Largest batch the persistent schedule takes (its per-sequence block prefix
+// lives in shared memory); larger batches use the fixed-partition schedule.
+constexpr int kPersistMaxSeqs = 2048;
+
+// Persistent kernel: stage ring + mbarriers + per-stage (unit, block) tags +
+// the block prefix cum[0..B] + alignment slack.
+constexpr int geo_persist_smem(int D, int BS, int B) {
+  return geo_warps(D, BS) * geo_stages(D, BS) * stage_bytes(D, BS) +
+         geo_warps(D, BS) * geo_stages(D, BS) * 16 + (B + 1) * 4 + 1024;
+}
+
 }  // namespace pkv

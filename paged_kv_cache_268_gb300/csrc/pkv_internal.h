@@ -20,8 +20,13 @@ struct DecodeArgs {
   const int32_t* block_tables;  // [B, MB]
   const int32_t* context_lens;  // [B]
   uint16_t* out;                // [B, Hq, D]
-  float* part_o;                // [B, Hq, S, D] un-normalised partial outputs
-  float2* part_ml;              // [B, Hq, S]   (running max in log2 units, sum)
+  float* part_o;                // un-normalised partial outputs: [B, Hq, S, D]
+                                // (split schedule) or [2 * warps, G, D] (persistent)
+  float2* part_ml;              // (running max in log2 units, sum) per partial row
+  int* hdr;                     // persistent schedule header: 4 x int64 (T, T1,
+                                // W1, C2), then cum[0..B] as int from int index 8
+  int g1;                       // persistent: CTAs of phase 1 (the rest are phase 2)
+  int f_per_mille;              // persistent: share of the list in phase 1 (x 1/1000)
   int* err;                     // device error word
   int B, Hq, Hkv, G, MB, NB;
   int S;                        // splits per sequence (grid extent)
@@ -41,16 +46,21 @@ struct KernelGeometry {
 // (group size 3..8).
 bool decode_geometry(int head_dim, int block_size, int variant, KernelGeometry* g);
 
-// Launch the decode grid (B * Hkv * S CTAs).  Returns cudaErrorInvalidValue
-// for an unbuilt combination.
+// Launch the decode kernel.  schedule 0: fixed partitions, grid B * Hkv * S;
+// schedule 1: persistent, `grid` CTAs.  Returns cudaErrorInvalidValue for an
+// unbuilt combination.
 cudaError_t launch_decode_f16_simt(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                   int head_dim, int block_size, cudaStream_t);
+                                   int head_dim, int block_size, int schedule, int grid,
+                                   cudaStream_t);
 cudaError_t launch_decode_bf16_simt(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                    int head_dim, int block_size, cudaStream_t);
+                                    int head_dim, int block_size, int schedule, int grid,
+                                    cudaStream_t);
 cudaError_t launch_decode_f16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                  int head_dim, int block_size, cudaStream_t);
+                                  int head_dim, int block_size, int schedule, int grid,
+                                  cudaStream_t);
 cudaError_t launch_decode_bf16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                   int head_dim, int block_size, cudaStream_t);
+                                   int head_dim, int block_size, int schedule, int grid,
+                                   cudaStream_t);
 
 int* device_error_word();  // device address of the error word (current device)
 

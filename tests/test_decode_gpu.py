@@ -33,9 +33,31 @@ def test_small_workloads(pkv, name, seed):
     assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), f"{name}/{seed}")
 
 
+def test_default_schedule_is_persistent(pkv):
+    for name in W.ORDER:
+        w = W.make(SMALL[name], seed=0)
+        d = device_inputs(w)
+        plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
+                                                w.max_context_len))
+        assert plan.schedule == 1 and plan.workspace_bytes > 0
+        assert plan.variant == (0 if w.spec.group <= 2 else 1)
+
+
+def test_large_batch_uses_partition_schedule(pkv):
+    """More than 2048 sequences fall back to the fixed-partition schedule."""
+    spec = W.scaled(W.WORKLOADS["llama3_8b_gqa"], 2100, 40)
+    w = W.make(spec, seed=9)
+    d = device_inputs(w)
+    plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
+                                            w.max_context_len))
+    assert plan.schedule == 0
+    assert_close(widen_out(gpu_decode(pkv, w, d)), oracle_decode(w), "B=2100")
+
+
 @pytest.mark.parametrize("split", [16, 64, 256, 512, 1 << 20])
 def test_split_count_invariance(pkv, split):
-    """Every split size gives the oracle's answer within tolerance."""
+    """Every partition size of the fixed-partition schedule gives the oracle's
+    answer within tolerance (split_tokens > 0 selects that schedule)."""
     for name in ("llama7b_mha", "long_ctx_gqa"):
         w = W.make(SMALL[name], seed=5)
         assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), oracle_decode(w),
@@ -51,18 +73,34 @@ def test_shape_sweep(pkv, dtype, G, D, bs):
     lens = np.array([1, bs - 1, bs, bs + 1, 3 * bs + 5], dtype=np.int32)
     spec = W.scaled(spec, 5, int(lens.max()))
     w = W.make(spec, seed=G * 1000 + D + bs, lens=lens)
-    for split in (0, bs):
+    for split in (0, bs):           # persistent schedule, then fixed partitions
         assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), oracle_decode(w),
                      f"G={G} D={D} bs={bs} split={split}")
 
 
 def test_edge_lengths(pkv):
-    """ctx = 1, multiples of the block size and one either side, long tails."""
+    """ctx = 1, multiples of the block size and one either side, long tails,
+    under both schedules."""
     lens = np.array([1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025], dtype=np.int32)
-    for base in ("llama7b_mha", "llama3_8b_gqa"):
+    for base in ("llama7b_mha", "llama3_8b_gqa", "long_ctx_gqa"):
         spec = W.scaled(W.WORKLOADS[base], len(lens), int(lens.max()))
         w = W.make(spec, seed=11, lens=lens)
-        assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), base)
+        ref = oracle_decode(w)
+        for split in (0, 512):
+            assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), ref,
+                         f"{base} split={split}")
+
+
+@pytest.mark.parametrize("B", [1, 3, 37])
+def test_persistent_few_blocks_and_many_warps(pkv, B):
+    """Batches with fewer KV blocks than warps in the grid, and single
+    sequences that every warp shares a piece of."""
+    rng = np.random.default_rng(B)
+    lens = rng.integers(1, 40 if B > 1 else 20000, size=B).astype(np.int32)
+    for base in ("llama7b_mha", "long_ctx_gqa"):
+        spec = W.scaled(W.WORKLOADS[base], B, int(lens.max()))
+        w = W.make(spec, seed=B, lens=lens)
+        assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), f"{base} B={B}")
 
 
 def test_all_context_one_returns_v(pkv):

@@ -44,7 +44,7 @@ def test_noalloc_matches_workspace_entry_point(pkv):
     for w in cases:                       # two calls in a row, different batches
         d = device_inputs(w)
         shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len)
-        assert pkv.decode_plan(shape).num_splits > 1      # the scratch is really used
+        assert pkv.decode_plan(shape).workspace_bytes > 0  # the scratch is really used
         out = torch.full_like(d["q"], float("nan"))
         assert _call_noalloc(pkv, d, out, w.scale, w.max_context_len) == 0
         ref = pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
