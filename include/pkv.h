@@ -79,8 +79,10 @@ enum {
  *   max_context_len     host-known upper bound on every context_lens[i]
  *                       (1 <= it <= MB * bs); sizes the split-KV grid
  *   dtype               pkv_dtype
- *   split_tokens        tokens per split-KV partition; 0 lets the library
- *                       choose; otherwise rounded up to a multiple of bs */
+ *   split_tokens        schedule choice: 0 lets the library choose the
+ *                       partition size; > 0 sets the tokens per split-KV
+ *                       partition (rounded up to a multiple of bs); -1 selects
+ *                       the persistent schedule (num_seqs <= 2048) */
 typedef struct {
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -95,13 +97,15 @@ typedef struct {
 } pkv_shape;
 
 /* How a decode call will run (filled by pkv_decode_plan).
- *   schedule 1 (default, split_tokens == 0 and num_seqs <= 2048): persistent
- *     kernel, grid_ctas = 2 per SM; every warp streams an equal share of all
- *     KV blocks of the batch, and a merge kernel combines the units a warp
- *     boundary cut.
- *   schedule 0 (split_tokens > 0, or larger batches): one CTA per (sequence,
- *     kv head, partition of split_tokens tokens), grid_ctas = B * Hkv * S,
- *     then a cross-partition reduce kernel when S > 1. */
+ *   schedule 0 (default): one CTA per (sequence, kv head, partition of
+ *     split_tokens tokens), grid_ctas = B * Hkv * S, dispatched by the
+ *     hardware as SMs free up, then a cross-partition reduce kernel when
+ *     S > 1.  With split_tokens == 0 the partition is 1024 tokens, or one
+ *     wave of equal partitions when the grid would be under four waves.
+ *   schedule 1 (split_tokens == -1, num_seqs <= 2048): persistent kernel;
+ *     every warp streams a fixed equal share of all KV blocks of the batch
+ *     (plus hardware-dispatched tail chunks), and a merge kernel combines the
+ *     units a share boundary cut. */
 typedef struct {
   int32_t schedule;
   int32_t split_tokens;     /* P, tokens per partition (schedule 0; else 0) */

@@ -190,6 +190,8 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
 
     q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables [B, MB] int32;
     context_lens [B] int32.  Returns out [B, Hq, D] (allocated if not given).
+    split_tokens: 0 = library's choice, > 0 = partition size, -1 = persistent
+    schedule.
     """
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _dense(t, n, q.dtype)

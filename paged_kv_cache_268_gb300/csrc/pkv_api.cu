@@ -241,7 +241,7 @@ int check_decode_shape(const pkv_shape* s) {
   int rc = check_cache_shape(s);
   if (rc != PKV_OK) return rc;
   if (s->num_seqs < 0 || s->num_q_heads < 1 || s->max_blocks_per_seq < 1 ||
-      s->max_context_len < 1 || s->split_tokens < 0)
+      s->max_context_len < 1 || s->split_tokens < -1)
     return PKV_ERR_INVALID;
   if (s->num_q_heads % s->num_kv_heads != 0) return PKV_ERR_INVALID;
   if (static_cast<long long>(s->max_context_len) >
@@ -264,14 +264,13 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   const bool persist_ok =
       s->num_seqs <= kPersistMaxSeqs &&
       static_cast<long long>(s->num_seqs) * s->max_blocks_per_seq * s->num_kv_heads < (1ll << 31);
-  if (s->split_tokens == 0 && persist_ok) {
+  if (s->split_tokens == -1 && persist_ok) {
     plan->schedule = 1;
     plan->split_tokens = 0;
     plan->num_splits = 0;
     const int f = phase1_per_mille();
     const int g2 = f == 1000 ? 0 : sms * phase2_ctas_per_sm();
-    plan->grid_ctas = sms * kPersistCtasPerSm + (g2 > 0 ? g2 : 0);
-    if (f < 1000 && g2 == 0) plan->grid_ctas = sms * kPersistCtasPerSm;
+    plan->grid_ctas = sms * kPersistCtasPerSm + g2;
     const size_t W = static_cast<size_t>(plan->grid_ctas) * geo.warps;
     plan->workspace_bytes = persist_hdr_bytes(s->num_seqs) + 2 * W * G * 8 +
                             2 * W * G * static_cast<size_t>(s->head_dim) * 4;
@@ -285,16 +284,17 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   if (s->split_tokens > 0) {
     P = (static_cast<long long>(s->split_tokens) + bs - 1) / bs * bs;
   } else {
-    // Default 512 tokens per partition (bounds the per-CTA tail); shrink it
-    // when the grid would not fill every SM twice over, never below one block
-    // per warp.
-    P = 512;
-    const long long want = 2LL * sms * 2;
-    if (units > 0 && units * ((maxL + P - 1) / P) < want) {
-      const long long S = (want + units - 1) / units;
+    // 1024-token partitions keep every CTA long enough to amortise its
+    // start-up while the hardware block scheduler balances the SMs.  When
+    // the whole grid would be under four waves, wave quantisation dominates
+    // instead: use exactly one wave of equal partitions.
+    const long long slots = static_cast<long long>(sms) * ctas_per_sm_for(geo.smem_bytes);
+    P = 1024;
+    if (units > 0 && units * ((maxL + P - 1) / P) < 4 * slots) {
+      const long long S = slots / units > 0 ? slots / units : 1;
       P = (maxL + S - 1) / S;
-      P = (P + gran - 1) / gran * gran;
     }
+    P = (P + gran - 1) / gran * gran;
     // At most 1024 partitions per sequence.
     const long long pmin = (static_cast<long long>(maxL) + 1023) / 1024;
     if (P < pmin) P = (pmin + gran - 1) / gran * gran;

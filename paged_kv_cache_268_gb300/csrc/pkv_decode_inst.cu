@@ -36,6 +36,7 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   if (schedule == 1) {
     constexpr int SMEM_MAX = geo_persist_smem(D, BS, kPersistMaxSeqs);
     static_assert(SMEM_MAX <= 113 * 1024, "two persistent CTAs must fit on one SM");
+    static_assert(ctas_per_sm_for(SMEM_MAX) >= 2, "two persistent CTAs must fit on one SM");
     auto kern = paged_decode_persistent<kBF, D, BS, NW, NS, Compute>;
     static int mask = 0;
     cudaError_t e = configure(kern, SMEM_MAX, &mask);

@@ -52,6 +52,7 @@ def _decode(lib, shape, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE, ws
     (dict(num_seqs=-1), -2),
     (dict(max_context_len=0), -2),
     (dict(max_context_len=129), -2),                     # > MB * bs
+    (dict(split_tokens=-2), -2),
     (dict(head_dim=96), -3),
     (dict(block_size=8), -3),
     (dict(dtype=5), -3),

@@ -33,25 +33,38 @@ def test_small_workloads(pkv, name, seed):
     assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), f"{name}/{seed}")
 
 
-def test_default_schedule_is_persistent(pkv):
+def test_schedule_selection(pkv):
+    """split_tokens 0 picks partitions, -1 the persistent schedule; the
+    tensor-core variant serves group sizes of 3 and more."""
     for name in W.ORDER:
         w = W.make(SMALL[name], seed=0)
         d = device_inputs(w)
-        plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
-                                                w.max_context_len))
-        assert plan.schedule == 1 and plan.workspace_bytes > 0
-        assert plan.variant == (0 if w.spec.group <= 2 else 1)
+        for split, sched in ((0, 0), (-1, 1), (64, 0)):
+            plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
+                                                    w.max_context_len, split))
+            assert plan.schedule == sched
+            assert plan.variant == (0 if w.spec.group <= 2 else 1)
+        assert plan.split_tokens == 64
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("name", W.ORDER)
+def test_persistent_schedule_small_workloads(pkv, name, seed):
+    w = W.make(SMALL[name], seed=seed)
+    assert_close(widen_out(gpu_decode(pkv, w, split_tokens=-1)), oracle_decode(w),
+                 f"persistent {name}/{seed}")
 
 
 def test_large_batch_uses_partition_schedule(pkv):
-    """More than 2048 sequences fall back to the fixed-partition schedule."""
+    """More than 2048 sequences fall back to the partition schedule even when
+    the persistent one is asked for."""
     spec = W.scaled(W.WORKLOADS["llama3_8b_gqa"], 2100, 40)
     w = W.make(spec, seed=9)
     d = device_inputs(w)
     plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
-                                            w.max_context_len))
+                                            w.max_context_len, -1))
     assert plan.schedule == 0
-    assert_close(widen_out(gpu_decode(pkv, w, d)), oracle_decode(w), "B=2100")
+    assert_close(widen_out(gpu_decode(pkv, w, d, split_tokens=-1)), oracle_decode(w), "B=2100")
 
 
 @pytest.mark.parametrize("split", [16, 64, 256, 512, 1 << 20])
@@ -73,7 +86,7 @@ def test_shape_sweep(pkv, dtype, G, D, bs):
     lens = np.array([1, bs - 1, bs, bs + 1, 3 * bs + 5], dtype=np.int32)
     spec = W.scaled(spec, 5, int(lens.max()))
     w = W.make(spec, seed=G * 1000 + D + bs, lens=lens)
-    for split in (0, bs):           # persistent schedule, then fixed partitions
+    for split in (0, bs, -1):       # auto partitions, one-block partitions, persistent
         assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), oracle_decode(w),
                      f"G={G} D={D} bs={bs} split={split}")
 
@@ -86,21 +99,24 @@ def test_edge_lengths(pkv):
         spec = W.scaled(W.WORKLOADS[base], len(lens), int(lens.max()))
         w = W.make(spec, seed=11, lens=lens)
         ref = oracle_decode(w)
-        for split in (0, 512):
+        for split in (0, 512, -1):
             assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), ref,
                          f"{base} split={split}")
 
 
 @pytest.mark.parametrize("B", [1, 3, 37])
-def test_persistent_few_blocks_and_many_warps(pkv, B):
-    """Batches with fewer KV blocks than warps in the grid, and single
-    sequences that every warp shares a piece of."""
+def test_few_blocks_and_single_long_sequence(pkv, B):
+    """Batches with fewer KV blocks than warps in the grid, and a single
+    long sequence that every CTA (or warp) takes a piece of."""
     rng = np.random.default_rng(B)
     lens = rng.integers(1, 40 if B > 1 else 20000, size=B).astype(np.int32)
     for base in ("llama7b_mha", "long_ctx_gqa"):
         spec = W.scaled(W.WORKLOADS[base], B, int(lens.max()))
         w = W.make(spec, seed=B, lens=lens)
-        assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), f"{base} B={B}")
+        ref = oracle_decode(w)
+        for split in (0, -1):
+            assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), ref,
+                         f"{base} B={B} split={split}")
 
 
 def test_all_context_one_returns_v(pkv):
@@ -171,13 +187,15 @@ def _sample_rows(w: W.Workload, n: int, rng) -> np.ndarray:
 
 @pytest.mark.parametrize("name", W.ORDER)
 def test_full_size_sampled(pkv, name):
-    """Full-size workloads in the benchmark's launch configuration; the oracle
-    recomputes a sample of (sequence, head) rows one by one."""
+    """Full-size workloads in the benchmark's launch configuration (and the
+    persistent schedule); the oracle recomputes a sample of (sequence, head)
+    rows one by one."""
     w = W.make(name, seed=0, device="cuda")
     d = device_inputs(w)
-    out = widen_out(gpu_decode(pkv, w, d))
     rows = _sample_rows(w, 48, np.random.default_rng(0))
     ref = oracle.decode_rows(rows, W.bits(w.q), W.bits(w.k_cache), W.bits(w.v_cache),
                              w.block_tables, w.context_lens, w.scale, w.spec.dtype)
-    assert_close(out[rows[:, 0], rows[:, 1]], ref, name)
-    assert np.all(np.isfinite(out))
+    for split in (0, -1):
+        out = widen_out(gpu_decode(pkv, w, d, split_tokens=split))
+        assert np.all(np.isfinite(out))
+        assert_close(out[rows[:, 0], rows[:, 1]], ref, f"{name} split={split}")
