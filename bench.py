@@ -180,53 +180,53 @@ def build_workload(args, rank: int, device):
     return W.make(spec, seed=args.seed + rank, device=device)
 
 
-def oracle_sample_rate(w: W.Workload, target_s: float, device, seed: int = 0):
-    """Time the CPU oracle on a bounded sample of (sequence, query head) rows of
-    the same workload; returns (GB/s of KV rows read, description)."""
-    import oracle  # test infrastructure: only the CPU-baseline / reference legs use it
+class OracleSampler:
+    """Times the CPU oracle on bounded samples of (sequence, query head) rows
+    of one workload.  The referenced K/V blocks are gathered to the host once;
+    each run() then computes a random sample of rows sized to a time budget."""
 
-    spec = w.spec
-    rng = np.random.default_rng(seed)
-    # calibrate on one row of a median-length sequence
-    order = np.argsort(w.context_lens)
-    mid = int(order[len(order) // 2])
-
-    def compact(seqs):
-        # gather the referenced blocks of the sampled sequences into a small pool
-        seqs = np.asarray(seqs)
-        nblk = -(-w.context_lens[seqs] // spec.block_size)
-        ids = np.concatenate([w.block_tables[s, :n] for s, n in zip(seqs, nblk)])
+    def __init__(self, w: W.Workload):
+        import oracle  # test infrastructure: only the CPU-baseline / reference legs use it
+        self.oracle = oracle
+        self.w = w
+        spec = w.spec
+        nblk = -(-w.context_lens // spec.block_size)
+        ids = np.concatenate([w.block_tables[i, :n] for i, n in enumerate(nblk)])
         uniq, inv = np.unique(ids, return_inverse=True)
         idx = torch.from_numpy(uniq.astype(np.int64)).to(w.k_cache.device)
-        kc = W.bits(w.k_cache.index_select(0, idx))
-        vc = W.bits(w.v_cache.index_select(0, idx))
-        tables = np.full((len(seqs), w.block_tables.shape[1]), -1, dtype=np.int32)
+        self.kc = W.bits(w.k_cache.index_select(0, idx))
+        self.vc = W.bits(w.v_cache.index_select(0, idx))
+        self.tables = np.full_like(w.block_tables, -1)
         k = 0
-        for r, n in enumerate(nblk):
-            tables[r, :n] = inv[k:k + n]
+        for i, n in enumerate(nblk):
+            self.tables[i, :n] = inv[k:k + n]
             k += n
-        return kc, vc, tables
+        self.q = W.bits(w.q)
+        mid = int(np.argsort(w.context_lens)[len(w.context_lens) // 2])
+        t0 = time.perf_counter()
+        self._rows(np.array([[mid, 0]], dtype=np.int32))
+        self.per_row = max(time.perf_counter() - t0, 1e-5)
 
-    qb = W.bits(w.q)
-    kc, vc, t = compact([mid])
-    t0 = time.perf_counter()
-    oracle.decode_rows([(0, 0)], qb[[mid]], kc, vc, t, w.context_lens[[mid]], w.scale, spec.dtype)
-    per_row = max(time.perf_counter() - t0, 1e-4)
-    nrows = int(max(1, min(spec.num_seqs * spec.num_q_heads, target_s / per_row)))
-    flat = rng.choice(spec.num_seqs * spec.num_q_heads, size=nrows, replace=False)
-    seqs = np.unique(flat // spec.num_q_heads)
-    kc, vc, tables = compact(seqs)
-    remap = {int(s): r for r, s in enumerate(seqs)}
-    rows = np.array([(remap[int(f // spec.num_q_heads)], int(f % spec.num_q_heads)) for f in flat],
-                    dtype=np.int32)
-    t0 = time.perf_counter()
-    oracle.decode_rows(rows, qb[seqs], kc, vc, tables, w.context_lens[seqs], w.scale, spec.dtype)
-    dt = time.perf_counter() - t0
-    # KV bytes a row reads: its L tokens of K and V for one kv head, shared by G q heads
-    kv = sum(int(w.context_lens[seqs[r]]) for r, _ in rows) * spec.head_dim * 2 * 2 / spec.group
-    desc = (f"{nrows} of {spec.num_seqs * spec.num_q_heads} (sequence, q head) rows of "
-            f"{spec.name}, single-threaded fp64 C oracle, {dt:.1f} s")
-    return kv / dt / 1e9, desc, dt
+    def _rows(self, rows):
+        w = self.w
+        return self.oracle.decode_rows(rows, self.q, self.kc, self.vc, self.tables,
+                                       w.context_lens, w.scale, w.spec.dtype)
+
+    def run(self, target_s: float, seed: int = 0):
+        """Returns (GB/s of KV rows read, description, seconds)."""
+        spec = self.w.spec
+        total = spec.num_seqs * spec.num_q_heads
+        nrows = int(max(1, min(total, target_s / self.per_row)))
+        flat = np.random.default_rng(seed).choice(total, size=nrows, replace=False)
+        rows = np.stack([flat // spec.num_q_heads, flat % spec.num_q_heads], axis=1).astype(np.int32)
+        t0 = time.perf_counter()
+        self._rows(rows)
+        dt = time.perf_counter() - t0
+        # KV bytes a row reads: its L tokens of K and V for one kv head, shared by G q heads
+        kv = float(self.w.context_lens[rows[:, 0]].astype(np.int64).sum()) * spec.head_dim * 4 / spec.group
+        desc = (f"{nrows} of {total} (sequence, q head) rows of {spec.name}, "
+                f"single-threaded fp64 C oracle, {dt:.2f} s")
+        return kv / dt / 1e9, desc, dt
 
 
 # ---------------------------------------------------------------- reference arm
@@ -235,12 +235,13 @@ def run_reference(args):
     if rank != 0:
         return 0
     spec = W.WORKLOADS[args.workload]
-    w = W.make(spec, seed=args.seed, device="cpu" if not torch.cuda.is_available() else "cuda")
+    w = W.make(spec, seed=args.seed, device="cuda" if torch.cuda.is_available() else "cpu")
+    sampler = OracleSampler(w)
     nsteps = args.steps + args.warmup
-    per_step = max(0.5, min(args.cpu_seconds, 150.0 / max(nsteps, 1)))
-    rates, times = [], []
+    per_step = min(args.cpu_seconds, 120.0 / max(nsteps, 1))   # whole run ~2 minutes at most
+    rates, times, desc = [], [], ""
     for i in range(nsteps):
-        gbs, desc, dt = oracle_sample_rate(w, per_step, None, seed=i)
+        gbs, desc, dt = sampler.run(per_step, seed=i)
         if i >= args.warmup:
             rates.append(gbs)
             times.append(dt)
@@ -402,7 +403,7 @@ def run_pkv(args):
 
     cpu = None
     if not args.no_cpu_baseline:
-        gbs, desc, _ = oracle_sample_rate(w, args.cpu_seconds, dev)
+        gbs, desc, _ = OracleSampler(w).run(args.cpu_seconds)
         cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
 
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
