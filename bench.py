@@ -168,6 +168,20 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def job_totals(dist, device, elapsed_ms: float, units: dict):
+    """Whole-job view of one timed region across replicas: the slowest rank's
+    time (MAX) and the sum over ranks of each unit count (every rank runs its
+    own seeded batch, so counts differ).  Without `dist` the local values."""
+    if dist is None:
+        return float(elapsed_ms), {k: float(v) for k, v in units.items()}
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    keys = sorted(units)
+    u = torch.tensor([float(units[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), {k: float(v) for k, v in zip(keys, u.tolist())}
+
+
 # ---------------------------------------------------------------- workload
 def build_workload(args, rank: int, device):
     spec = W.WORKLOADS[args.workload]
@@ -338,15 +352,14 @@ def run_pkv(args):
     total_ms = start.elapsed_time(end)
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     append_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     assert pkv.get_device_error() == 0
 
     kv_bytes = w.kv_bytes()
+    total_ms, job = job_totals(dist, dev, total_ms,
+                               {"kv_bytes": kv_bytes, "seqs": spec.num_seqs,
+                                "ctx_tokens": int(w.context_lens.sum())})
     ms_per_step = total_ms / K
-    value = ws * kv_bytes * K / (total_ms * 1e-3) / 1e9
+    value = job["kv_bytes"] * K / (total_ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     dec_avg = sum(decode_ms) / K
     achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
@@ -386,13 +399,9 @@ def run_pkv(args):
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms, ejob = job_totals(dist, dev, s0.elapsed_time(s1), {"kv_bytes": kv_bytes})
         assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
-        e2e = {"value": ws * kv_bytes * Ke / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+        e2e = {"value": ejob["kv_bytes"] * Ke / (e_ms * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                "ms_per_step": e_ms / Ke}
 
@@ -426,8 +435,8 @@ def run_pkv(args):
                    "l2": f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB L2)",
                    "parallelism": f"replicas x{ws}"},
         "pct_hbm_peak": value / ws / peak,
-        "seq_tokens_per_s": ws * spec.num_seqs * K / (total_ms * 1e-3),
-        "context_tokens_per_s": ws * int(w.context_lens.sum()) * K / (total_ms * 1e-3),
+        "seq_tokens_per_s": job["seqs"] * K / (total_ms * 1e-3),
+        "context_tokens_per_s": job["ctx_tokens"] * K / (total_ms * 1e-3),
         "decode_ms_median": statistics.median(decode_ms),
         "decode_ms_p90": float(np.percentile(decode_ms, 90)),
         "append_us_median": 1e3 * statistics.median(append_ms),
