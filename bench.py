@@ -57,6 +57,9 @@ def parse_args(argv=None):
                    help="shrink the batch (and pool) for profiler captures; 0 = full workload")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--split-tokens", type=int, default=0)
+    p.add_argument("--two-call", action="store_true",
+                   help="time kv_cache_append + paged_attn_decode as two calls instead of "
+                        "the fused decode_step")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -311,10 +314,15 @@ def run_pkv(args):
     ws_buf = pkv.alloc_workspace(shape, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
-        pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
-                              split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+    def step(k_in=k_new, v_in=v_new, s_in=slots, q_in=q, bt_in=bt, cl_in=cl):
+        if args.two_call:
+            pkv.kv_cache_append(k_in, v_in, s_in, kc, vc, stream=stream)
+            pkv.paged_attn_decode(q_in, kc, vc, bt_in, cl_in, w.scale, out, max_context_len=maxL,
+                                  split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+        else:
+            pkv.decode_step(q_in, k_in, v_in, kc, vc, bt_in, cl_in, w.scale, out,
+                            max_context_len=maxL, split_tokens=args.split_tokens,
+                            workspace=ws_buf, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -336,10 +344,14 @@ def run_pkv(args):
     for i in range(K):
         a, b, c = ev[i]
         a.record(stream)
-        pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
-        b.record(stream)
-        pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
-                              split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+        if args.two_call:
+            pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
+            b.record(stream)
+            pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
+                                  split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+        else:
+            b.record(stream)
+            step()
         c.record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -375,15 +387,16 @@ def run_pkv(args):
         h_out = torch.empty_like(h_q).pin_memory()
         d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
         d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
+        pairs = [(d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_cl, h_cl)]
+        if args.two_call:
+            pairs.append((d_slots, h_slots))      # the fused step derives the slots itself
+        h2d = sum(h.numel() * h.element_size() for _, h in pairs)
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step():
-            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_bt, h_bt), (d_cl, h_cl)):
+            for d, h in pairs:
                 d.copy_(h, non_blocking=True)
-            pkv.kv_cache_append(d_k, d_v, d_slots, kc, vc, stream=stream)
-            pkv.paged_attn_decode(d_q, kc, vc, d_bt, d_cl, w.scale, out, max_context_len=maxL,
-                                  split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+            step(d_k, d_v, d_slots, d_q, d_bt, d_cl)
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -427,7 +440,8 @@ def run_pkv(args):
                    "head_dim": spec.head_dim, "block_size": spec.block_size,
                    "pool_blocks": spec.num_blocks, "context_lens": f"{spec.lens}{tuple(spec.len_args)}",
                    "sum_context_len": int(w.context_lens.sum()), "seed": args.seed,
-                   "step": "kv_cache_append(1 token/seq) + paged_attn_decode",
+                   "step": ("kv_cache_append(1 token/seq) + paged_attn_decode" if args.two_call
+                            else "decode_step: append of 1 token/seq fused into paged decode"),
                    "schedule": "persistent" if plan.schedule == 1 else "partitions",
                    "grid_ctas": plan.grid_ctas,
                    "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
@@ -439,8 +453,10 @@ def run_pkv(args):
         "context_tokens_per_s": job["ctx_tokens"] * K / (total_ms * 1e-3),
         "decode_ms_median": statistics.median(decode_ms),
         "decode_ms_p90": float(np.percentile(decode_ms, 90)),
-        "append_us_median": 1e3 * statistics.median(append_ms),
-        "roofline": {"bound": "hbm", "kernel": "paged_attn_decode (decode + merge kernels)",
+        "append_us_median": 1e3 * statistics.median(append_ms) if args.two_call else None,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged_attn_decode" if args.two_call else "decode_step")
+                               + " (decode kernel + split reduce)",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes},

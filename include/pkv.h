@@ -166,6 +166,29 @@ int pkv_paged_attn_decode(const pkv_shape* shape, const void* q,
                           pkv_stream_t stream);
 
 /*
+ * One continuous-batching decode step in one launch (the append fused into
+ * the decode): for every sequence i, this step's token (k_new[i], v_new[i])
+ * is written at position L - 1, i.e. slot
+ *     block_tables[i][(L-1) / bs] * bs + (L-1) % bs,
+ * then decode attention runs over all L = context_lens[i] tokens.  The result
+ * equals pkv_kv_cache_append with that slot mapping followed by
+ * pkv_paged_attn_decode, bit for bit, caches included.  Per-iteration
+ * metadata update plus attention over the block table (third page,
+ * "continuous batching" and "PagedAttention" sections).
+ *
+ *   k_new, v_new  [B, Hkv, D], 16-byte aligned
+ *   other arguments as pkv_paged_attn_decode; k_cache and v_cache are written
+ * The block that receives a sequence's new token must not be referenced by
+ * another sequence of the batch (copy it first when a prefix block is shared).
+ * Runs the partition schedule; split_tokens == -1 gives PKV_ERR_UNSUPPORTED.
+ */
+int pkv_decode_step(const pkv_shape* shape, const void* q, const void* k_new,
+                    const void* v_new, void* k_cache, void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens,
+                    float scale, void* out, void* workspace, size_t workspace_bytes,
+                    pkv_stream_t stream);
+
+/*
  * pkv_paged_attn_decode for callers that cannot allocate device memory.  The
  * pages have no counterpart to this call; it exists for callers that own all
  * device memory themselves (an engine that reserved HBM for its KV block pool

@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     alloc_workspace,
     decode_plan,
     decode_shape,
+    decode_step,
     get_device_error,
     kv_cache_append,
     launch_count,

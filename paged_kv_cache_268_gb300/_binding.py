@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
     lib.pkv_kv_cache_append.restype = ctypes.c_int
     lib.pkv_paged_attn_decode.argtypes = [sp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.pkv_paged_attn_decode.restype = ctypes.c_int
+    lib.pkv_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
+    lib.pkv_decode_step.restype = ctypes.c_int
     lib.pkv_decode_plan.argtypes = [sp, ctypes.POINTER(Plan)]
     lib.pkv_decode_plan.restype = ctypes.c_int
     lib.pkv_workspace_bytes.argtypes = [sp, ctypes.POINTER(sz)]
@@ -215,6 +217,38 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                      _ptr(out), _ptr(workspace),
                                      0 if workspace is None else workspace.numel(),
                                      _stream_ptr(stream)))
+    return out
+
+
+def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None, *,
+                max_context_len: int | None = None, split_tokens: int = 0,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Append this step's token (k_new, v_new: [B, Hkv, D]) at position L-1 of
+    every sequence and run decode attention, in one launch (plus the reduce)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache")):
+        _dense(t, n, q.dtype)
+    _dense(block_tables, "block_tables", torch.int32)
+    _dense(context_lens, "context_lens", torch.int32)
+    NB, Hkv, bs, D = _cache_shape(k_cache)
+    if k_new.shape != (q.shape[0], Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new, v_new must be [B, Hkv, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _dense(out, "out", q.dtype)
+    shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens)
+    if workspace is None:
+        workspace = alloc_workspace(shape, q.device)
+    _check("pkv_decode_step",
+           load_library().pkv_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                          _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                          _ptr(context_lens), float(scale), _ptr(out),
+                                          _ptr(workspace),
+                                          0 if workspace is None else workspace.numel(),
+                                          _stream_ptr(stream)))
     return out
 
 

@@ -396,11 +396,13 @@ extern "C" int pkv_kv_cache_append(const pkv_shape* s, const void* k, const void
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const void* k_cache,
-                                     const void* v_cache, const int32_t* block_tables,
-                                     const int32_t* context_lens, float scale, void* out,
-                                     void* workspace, size_t workspace_bytes,
-                                     pkv_stream_t stream) {
+namespace {
+
+// Shared body of pkv_paged_attn_decode and pkv_decode_step (k_new != null).
+int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
+                void* workspace, size_t workspace_bytes, pkv_stream_t stream, const void* k_new,
+                const void* v_new) {
   int rc = check_decode_shape(s);
   if (rc != PKV_OK) return rc;
   if (s->num_seqs == 0) return PKV_OK;
@@ -414,6 +416,7 @@ extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const vo
   pkv_plan plan{};
   rc = make_plan(s, d->sms, &plan);
   if (rc != PKV_OK) return rc;
+  if (k_new && plan.schedule != 0) return PKV_ERR_UNSUPPORTED;
   if (plan.workspace_bytes > 0) {
     if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16))
       return PKV_ERR_WORKSPACE;
@@ -446,6 +449,10 @@ extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const vo
                                      : nullptr;
   }
   a.err = d->err;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_cache = static_cast<uint16_t*>(const_cast<void*>(k_cache));
+  a.v_cache = static_cast<uint16_t*>(const_cast<void*>(v_cache));
   a.B = s->num_seqs;
   a.Hq = s->num_q_heads;
   a.Hkv = s->num_kv_heads;
@@ -481,6 +488,29 @@ extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const vo
     g_launches.fetch_add(1);
   }
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_attn_decode(const pkv_shape* s, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, float scale, void* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     pkv_stream_t stream) {
+  return decode_impl(s, q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                     workspace_bytes, stream, nullptr, nullptr);
+}
+
+extern "C" int pkv_decode_step(const pkv_shape* s, const void* q, const void* k_new,
+                               const void* v_new, void* k_cache, void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, void* out, void* workspace, size_t workspace_bytes,
+                               pkv_stream_t stream) {
+  if (!s) return PKV_ERR_NULL;
+  if (s->num_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_NULL;
+  if (s->num_seqs > 0 && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_ALIGN;
+  return decode_impl(s, q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                     workspace_bytes, stream, k_new, v_new);
 }
 
 extern "C" int pkv_get_device_error(int32_t* code, pkv_stream_t stream) {

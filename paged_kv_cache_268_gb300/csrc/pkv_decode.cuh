@@ -498,6 +498,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int jb = j0 + warp + NW * k;
     const int valid = min(BS, L - jb * BS);
     const uint32_t kt = wbuf + st * STAGE;
+    if (a.k_new != nullptr && jb == (L - 1) / BS) {
+      // Fused append: this step's token (position L-1) goes to its slot in
+      // the cache and, since the tile was staged before, into the tile too.
+      const int r = (L - 1) - jb * BS;
+      const size_t src = ((size_t)seq * a.Hkv + kvh) * D;
+      const size_t dst = (((size_t)ids[jb - j0] * a.Hkv + kvh) * BS + r) * D;
+      for (int c = lane; c < 2 * (D / 8); c += 32) {
+        const bool isv = c >= D / 8;
+        const int gc = isv ? c - D / 8 : c;
+        const uint4 x = *reinterpret_cast<const uint4*>((isv ? a.v_new : a.k_new) + src + gc * 8);
+        const uint32_t sa = (isv ? kt + TILE : kt) + tile_off<BS>(r, gc);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sa), "r"(x.x), "r"(x.y),
+                     "r"(x.z), "r"(x.w)
+                     : "memory");
+        *reinterpret_cast<uint4*>((isv ? a.v_cache : a.k_cache) + dst + gc * 8) = x;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     cs.block(kt, kt + TILE, valid, a.scale_log2, lane);
     __syncwarp();
     if (lane == 0 && k + NS < my_n) {

@@ -25,6 +25,10 @@ struct DecodeArgs {
   float2* part_ml;              // (running max in log2 units, sum) per partial row
   int* hdr;                     // persistent schedule header: 4 x int64 (T, T1,
                                 // W1, C2), then cum[0..B] as int from int index 8
+  const uint16_t* k_new;        // fused append: this step's K/V rows [B, Hkv, D],
+  const uint16_t* v_new;        //   or null for a plain decode
+  uint16_t* k_cache;            // fused append: the caches the rows go to
+  uint16_t* v_cache;
   int g1;                       // persistent: CTAs of phase 1 (the rest are phase 2)
   int f_per_mille;              // persistent: share of the list in phase 1 (x 1/1000)
   int* err;                     // device error word

@@ -1,0 +1,85 @@
+"""pkv_decode_step (append fused into the decode launch) through the C ABI:
+bit-identical caches and outputs to pkv_kv_cache_append + pkv_paged_attn_decode,
+and the oracle's append-then-decode within tolerance."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_268_gb300 import workloads as W
+from parity import assert_close, device_inputs, oracle_decode, widen_out
+from test_decode_gpu import SMALL
+
+pytestmark = pytest.mark.gpu
+
+
+def _two_call(pkv, w, d):
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    pkv.kv_cache_append(w.k_new.cuda(), w.v_new.cuda(), torch.from_numpy(w.slot_mapping).cuda(),
+                        kc, vc)
+    out = pkv.paged_attn_decode(d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                max_context_len=w.max_context_len)
+    return out, kc, vc
+
+
+def _fused(pkv, w, d, split_tokens=0):
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    out = pkv.decode_step(d["q"], w.k_new.cuda(), w.v_new.cuda(), kc, vc, d["block_tables"],
+                          d["context_lens"], w.scale, max_context_len=w.max_context_len,
+                          split_tokens=split_tokens)
+    return out, kc, vc
+
+
+def _same(a, b):
+    return torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("name", W.ORDER)
+def test_fused_step_matches_two_calls_and_oracle(pkv, name, seed):
+    w = W.make(SMALL[name], seed=seed)
+    d = device_inputs(w)
+    o2, k2, v2 = _two_call(pkv, w, d)
+    for split in (0, 16 if w.spec.block_size == 16 else 32):
+        of, kf, vf = _fused(pkv, w, d, split)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert _same(kf, k2) and _same(vf, v2), "caches differ from append + decode"
+        if split == 0:
+            assert _same(of, o2), "output differs from append + decode"
+    ek, ev = oracle.append(W.bits(w.k_new), W.bits(w.v_new), w.slot_mapping,
+                           W.bits(w.k_cache), W.bits(w.v_cache))
+    assert np.array_equal(W.bits(kf), ek) and np.array_equal(W.bits(vf), ev)
+    assert_close(widen_out(of), oracle_decode(w, ek, ev), f"fused {name}/{seed}")
+
+
+def test_fused_step_lengths_one_and_block_edges(pkv):
+    lens = np.array([1, 16, 17, 32, 33, 1024, 1025], dtype=np.int32)
+    for base in ("llama7b_mha", "llama3_8b_gqa", "long_ctx_gqa"):
+        spec = W.scaled(W.WORKLOADS[base], len(lens), int(lens.max()))
+        w = W.make(spec, seed=5, lens=lens)
+        d = device_inputs(w)
+        o2, k2, v2 = _two_call(pkv, w, d)
+        of, kf, vf = _fused(pkv, w, d)
+        torch.cuda.synchronize()
+        assert _same(kf, k2) and _same(vf, v2) and _same(of, o2), base
+
+
+def test_fused_step_full_continuous_batching(pkv):
+    w = W.make("cont_batch", seed=0, device="cuda")
+    d = device_inputs(w)
+    o2, k2, v2 = _two_call(pkv, w, d)
+    of, kf, vf = _fused(pkv, w, d)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert _same(kf, k2) and _same(vf, v2) and _same(of, o2)
+
+
+def test_fused_step_rejects_persistent_schedule(pkv):
+    w = W.make(SMALL["llama7b_mha"], seed=0)
+    d = device_inputs(w)
+    with pytest.raises(pkv.PkvError) as e:
+        _fused(pkv, w, d, split_tokens=-1)
+    assert e.value.code == -3
