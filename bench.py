@@ -60,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--two-call", action="store_true",
                    help="time kv_cache_append + paged_attn_decode as two calls instead of "
                         "the fused decode_step")
+    p.add_argument("--copy-bench", action="store_true",
+                   help="also time pkv_copy_blocks (device->device, device->pinned host, "
+                        "pinned host->device) on blocks of this workload's shape")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -246,6 +249,40 @@ class OracleSampler:
         return kv / dt / 1e9, desc, dt
 
 
+def copy_bench(pkv, spec, dev, stream, n_pairs=1024, reps=20):
+    """GB/s of pkv_copy_blocks moving n_pairs whole blocks (K and V, every kv
+    head): within the GPU pool, GPU -> pinned host pool, pinned host -> GPU."""
+    shape = (4 * n_pairs, spec.num_kv_heads, spec.block_size, spec.head_dim)
+    dt = torch.float16 if spec.dtype == W.F16 else torch.bfloat16
+    gk, gv = torch.zeros(shape, dtype=dt, device=dev), torch.zeros(shape, dtype=dt, device=dev)
+    hshape = (n_pairs,) + shape[1:]
+    hk, hv = torch.zeros(hshape, dtype=dt).pin_memory(), torch.zeros(hshape, dtype=dt).pin_memory()
+    rng = np.random.default_rng(0)
+    src = rng.permutation(shape[0])[:n_pairs]
+    dst = rng.permutation(np.setdiff1d(np.arange(shape[0]), src))[:n_pairs]
+    ppairs = {"device_to_device": np.stack([src, dst], 1),
+              "device_to_host": np.stack([src, rng.permutation(n_pairs)], 1),
+              "host_to_device": np.stack([rng.permutation(n_pairs), dst], 1)}
+    pools = {"device_to_device": (gk, gv, gk, gv), "device_to_host": (gk, gv, hk, hv),
+             "host_to_device": (hk, hv, gk, gv)}
+    nbytes = n_pairs * 2 * gk[0].numel() * gk.element_size()
+    res = {"pairs": n_pairs, "bytes_per_call": nbytes}
+    for name, pr in ppairs.items():
+        p = torch.from_numpy(pr.astype(np.int32)).to(dev)
+        for _ in range(3):
+            pkv.copy_blocks(*pools[name], p, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            pkv.copy_blocks(*pools[name], p, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name + "_gbs"] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    assert pkv.get_device_error() == 0
+    return res
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     ws, rank, local = dist_env()
@@ -423,6 +460,7 @@ def run_pkv(args):
             dist.destroy_process_group()
         return 0
 
+    copy_res = copy_bench(pkv, spec, dev, stream) if args.copy_bench else None
     cpu = None
     if not args.no_cpu_baseline:
         gbs, desc, _ = OracleSampler(w).run(args.cpu_seconds)
@@ -463,6 +501,7 @@ def run_pkv(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
+        "block_copy": copy_res,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

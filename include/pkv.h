@@ -55,7 +55,8 @@ enum {
   PKV_ERR_ALIGN = -4,        /* a pointer is not aligned as the layout requires */
   PKV_ERR_WORKSPACE = -5,    /* workspace missing or smaller than required */
   PKV_ERR_CUDA = -6,         /* a CUDA runtime/driver call failed */
-  PKV_ERR_DEVICE = -7        /* reserved: a kernel recorded a device-side error */
+  PKV_ERR_DEVICE = -7,       /* reserved: a kernel recorded a device-side error */
+  PKV_ERR_NO_BLOCKS = -8     /* block manager: the pool has no free block left */
 };
 
 /* Device-side error codes (pkv_get_device_error). */
@@ -209,6 +210,94 @@ int pkv_paged_attn_decode_noalloc(const pkv_shape* shape, const void* q,
                                   const int32_t* block_tables,
                                   const int32_t* context_lens, float scale,
                                   void* out, pkv_stream_t stream);
+
+/*
+ * Whole-block copy between two pools of the same block shape: for i in
+ * [0, num_pairs), block pairs[2i] of (src_k, src_v) is copied to block
+ * pairs[2i+1] of (dst_k, dst_v), every kv head.  Serves copy-on-write inside
+ * the GPU pool and the swap-out / swap-in of the tiered cache (first page,
+ * section 4.2: cold blocks move to pinned CPU memory and come back by DMA).
+ * Bit-exact.
+ *
+ *   shape        uses num_kv_heads, head_dim, block_size, dtype
+ *   src_*, dst_* [num_blocks, Hkv, bs, D] pools, 16-byte aligned, readable /
+ *                writable by the GPU: device memory, or pinned host memory
+ *                (cudaHostAlloc / cudaMallocHost), which the GPU reaches
+ *                through its host pointer under unified addressing
+ *   pairs        [num_pairs][2] int32, device-readable
+ * Pairs with an id outside its pool are skipped and set PKV_DEV_BAD_BLOCK_ID.
+ * Destination blocks must be distinct and must not be sources in the same
+ * call.  num_pairs == 0 is a no-op.
+ */
+int pkv_copy_blocks(const pkv_shape* shape, const void* src_k, const void* src_v,
+                    int32_t src_num_blocks, void* dst_k, void* dst_v,
+                    int32_t dst_num_blocks, const int32_t* pairs, int32_t num_pairs,
+                    pkv_stream_t stream);
+
+/*
+ * Block manager (host only, no GPU calls): the bookkeeping side of the paged
+ * cache (first page, section 4.2: fixed-size blocks handed out on demand,
+ * allocate(seq, num_tokens) takes ceil(num_tokens / block_size) blocks; the
+ * tiered variant keeps the last gpu_window blocks of a sequence on the GPU
+ * and moves older ones to pinned CPU memory), updated between launches as
+ * sequences join, grow and leave (third page, "continuous batching").
+ * Sequences made by pkv_bm_fork share their parent's blocks (reference
+ * counted); writing into a shared block first copies it (copy-on-write).
+ * Every call is thread-safe and returns PKV_OK or a negative PKV_ERR_*;
+ * a call that fails changes nothing.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of num_gpu_blocks GPU blocks and num_cpu_blocks CPU blocks of
+ * block_size tokens.  Each pool's free list is a stack: initially ids come
+ * out lowest first, later the most recently freed block is reused first.
+ * NULL on bad sizes. */
+pkv_block_manager* pkv_bm_create(int32_t num_gpu_blocks, int32_t num_cpu_blocks,
+                                 int32_t block_size);
+void pkv_bm_destroy(pkv_block_manager* m);
+
+/* New sequence holding num_tokens tokens (ceil(num_tokens / bs) GPU blocks).
+ * PKV_ERR_INVALID if seq_id exists, PKV_ERR_NO_BLOCKS if the pool is short. */
+int pkv_bm_add_sequence(pkv_block_manager* m, int64_t seq_id, int32_t num_tokens);
+
+/* New sequence `child` sharing every block of `parent` (all on the GPU). */
+int pkv_bm_fork(pkv_block_manager* m, int64_t parent, int64_t child);
+
+/* Reserve the slot of the sequence's next token: *slot = block * bs + offset.
+ * When that token lands in a block shared with another sequence, the
+ * sequence first gets a fresh block: *copy_src / *copy_dst name the GPU
+ * blocks to copy (pkv_copy_blocks) before writing; both are -1 otherwise. */
+int pkv_bm_append_token(pkv_block_manager* m, int64_t seq_id, int32_t* slot,
+                        int32_t* copy_src, int32_t* copy_dst);
+
+/* Drop the sequence; blocks no other sequence references become free. */
+int pkv_bm_free_sequence(pkv_block_manager* m, int64_t seq_id);
+
+/* Move the sequence's blocks older than its last gpu_window blocks (those on
+ * the GPU and not shared) to the CPU pool.  Writes num_pairs (gpu id, cpu id)
+ * pairs for pkv_copy_blocks (GPU pool -> CPU pool) into pairs[2 * max_pairs].
+ * The GPU blocks are free again as soon as this returns: enqueue the copy
+ * before any launch that may write into reused blocks (same stream). */
+int pkv_bm_swap_out(pkv_block_manager* m, int64_t seq_id, int32_t gpu_window,
+                    int32_t* pairs, int32_t max_pairs, int32_t* num_pairs);
+
+/* Bring every CPU block of the sequence back to the GPU pool: (cpu id,
+ * gpu id) pairs for pkv_copy_blocks (CPU pool -> GPU pool). */
+int pkv_bm_swap_in(pkv_block_manager* m, int64_t seq_id, int32_t* pairs,
+                   int32_t max_pairs, int32_t* num_pairs);
+
+int pkv_bm_num_free(pkv_block_manager* m, int32_t* gpu_blocks, int32_t* cpu_blocks);
+
+int pkv_bm_seq_info(pkv_block_manager* m, int64_t seq_id, int32_t* num_tokens,
+                    int32_t* num_blocks, int32_t* num_cpu_blocks);
+
+/* Fill a decode batch's host arrays: block_tables [n, max_blocks_per_seq]
+ * (-1 past each sequence's blocks) and context_lens [n].  PKV_ERR_INVALID if
+ * a sequence is unknown, has CPU-resident blocks, or needs more than
+ * max_blocks_per_seq blocks. */
+int pkv_bm_block_tables(pkv_block_manager* m, const int64_t* seq_ids, int32_t n,
+                        int32_t max_blocks_per_seq, int32_t* block_tables,
+                        int32_t* context_lens);
 
 /* Validate `shape` and report how pkv_paged_attn_decode will run on the
  * current device (split size, kernel variant, workspace size).  Host only;

@@ -82,6 +82,8 @@ def _bind(lib):
     lib.pkv_oracle_append.argtypes = [i, i, i, i, i, u16p, u16p, i32p, u16p,
                                       u16p]
     lib.pkv_oracle_append.restype = i
+    lib.pkv_oracle_copy_blocks.argtypes = [i, i, i, i, i, i, u16p, u16p, i32p]
+    lib.pkv_oracle_copy_blocks.restype = i
     return lib
 
 
@@ -176,3 +178,19 @@ def append(k, v, slot_mapping, k_cache, v_cache, lib=None):
     if bad != 0:
         raise ValueError(f"oracle: {bad} slots outside the pool")
     return kc, vc
+
+
+def copy_blocks(src, dst, pairs, lib=None):
+    """Return a copy of pool `dst` with block pairs[i, 0] of pool `src` copied
+    to block pairs[i, 1] (pools [NB, Hkv, bs, D] of 16-bit patterns)."""
+    lib = lib or load()
+    src = _u16(src)
+    out = _u16(dst).copy()
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    _, Hkv, bs, D = src.shape
+    bad = lib.pkv_oracle_copy_blocks(pr.shape[0], Hkv, bs, D, src.shape[0], out.shape[0],
+                                     _ptr(src, ctypes.c_uint16), _ptr(out, ctypes.c_uint16),
+                                     _ptr(pr, ctypes.c_int32))
+    if bad != 0:
+        raise ValueError(f"oracle: {bad} pairs outside the pools")
+    return out

@@ -22,6 +22,11 @@
  *
  *   Grouped-query heads: query head h reads kv head h / (Hq / Hkv).
  *
+ *   Block copy: block pairs[2i] of a source pool is copied to block
+ *   pairs[2i+1] of a destination pool, every kv head, K and V (the swap and
+ *   copy-on-write moves of the tiered block manager, section 4.2 of the first
+ *   page).
+ *
  *   KV append: each new token's K/V row is written into slot s of the cache,
  *   block s / block_size, row s % block_size (block manager allocation,
  *   section 4.2 of the first page, 0539edu.com news 6031734; per-iteration
@@ -188,6 +193,22 @@ int pkv_oracle_append(int T, int Hkv, int D, int bs, int NB,
                 v_cache[dst + d] = v[src + d];
             }
         }
+    }
+    return bad;
+}
+
+/* Block copy: for each pair i, block pairs[2i] of src (a pool of src_nb blocks
+ * of Hkv * bs * D elements) is copied to block pairs[2i+1] of dst (dst_nb
+ * blocks).  Returns the number of pairs with an id outside its pool (those are
+ * skipped). */
+int pkv_oracle_copy_blocks(int n_pairs, int Hkv, int bs, int D, int src_nb, int dst_nb,
+                           const uint16_t* src, uint16_t* dst, const int32_t* pairs) {
+    size_t per = (size_t)Hkv * bs * D;
+    int bad = 0;
+    for (int i = 0; i < n_pairs; ++i) {
+        int s = pairs[2 * i], d = pairs[2 * i + 1];
+        if (s < 0 || s >= src_nb || d < 0 || d >= dst_nb) { ++bad; continue; }
+        for (size_t e = 0; e < per; ++e) dst[(size_t)d * per + e] = src[(size_t)s * per + e];
     }
     return bad;
 }

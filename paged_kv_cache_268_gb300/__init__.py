@@ -6,7 +6,9 @@ seeded workload generator used by the tests and the benchmark.  Build the
 library with ``python -m paged_kv_cache_268_gb300.build``.
 """
 from ._binding import (  # noqa: F401
+    BlockManager,
     PkvError,
+    copy_blocks,
     alloc_workspace,
     decode_plan,
     decode_shape,

@@ -67,6 +67,25 @@ def load_library(path: str | None = None):
     lib.pkv_paged_attn_decode.restype = ctypes.c_int
     lib.pkv_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.pkv_decode_step.restype = ctypes.c_int
+    lib.pkv_copy_blocks.argtypes = [sp, vp, vp, i32, vp, vp, i32, vp, i32, vp]
+    lib.pkv_copy_blocks.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.pkv_bm_create.argtypes = [i32, i32, i32]
+    lib.pkv_bm_create.restype = vp
+    lib.pkv_bm_destroy.argtypes = [vp]
+    lib.pkv_bm_destroy.restype = None
+    lib.pkv_bm_add_sequence.argtypes = [vp, i64, i32]
+    lib.pkv_bm_fork.argtypes = [vp, i64, i64]
+    lib.pkv_bm_append_token.argtypes = [vp, i64, i32p, i32p, i32p]
+    lib.pkv_bm_free_sequence.argtypes = [vp, i64]
+    lib.pkv_bm_swap_out.argtypes = [vp, i64, i32, i32p, i32, i32p]
+    lib.pkv_bm_swap_in.argtypes = [vp, i64, i32p, i32, i32p]
+    lib.pkv_bm_num_free.argtypes = [vp, i32p, i32p]
+    lib.pkv_bm_seq_info.argtypes = [vp, i64, i32p, i32p, i32p]
+    lib.pkv_bm_block_tables.argtypes = [vp, ctypes.POINTER(i64), i32, i32, i32p, i32p]
+    for n in ("add_sequence", "fork", "append_token", "free_sequence", "swap_out", "swap_in",
+              "num_free", "seq_info", "block_tables"):
+        getattr(lib, "pkv_bm_" + n).restype = ctypes.c_int
     lib.pkv_decode_plan.argtypes = [sp, ctypes.POINTER(Plan)]
     lib.pkv_decode_plan.restype = ctypes.c_int
     lib.pkv_workspace_bytes.argtypes = [sp, ctypes.POINTER(sz)]
@@ -250,6 +269,105 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                                           0 if workspace is None else workspace.numel(),
                                           _stream_ptr(stream)))
     return out
+
+
+def copy_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                dst_v: torch.Tensor, pairs: torch.Tensor, stream=None) -> None:
+    """Copy block pairs[i, 0] of (src_k, src_v) to block pairs[i, 1] of
+    (dst_k, dst_v).  Pools are [NB, Hkv, bs, D] tensors on the GPU or in
+    pinned host memory; pairs is an int32 [n, 2] tensor the GPU can read."""
+    for t, n in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v")):
+        if not t.is_contiguous() or t.dim() != 4 or t.dtype != src_k.dtype:
+            raise ValueError(f"{n} must be a contiguous [NB, Hkv, bs, D] tensor of one dtype")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must live on the GPU or in pinned host memory")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_v.shape != src_k.shape or dst_v.shape != dst_k.shape:
+        raise ValueError("pools must share the block shape")
+    if pairs.dtype != torch.int32 or not pairs.is_contiguous() or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be a contiguous int32 [n, 2] tensor")
+    if not (pairs.is_cuda or pairs.is_pinned()):
+        raise ValueError("pairs must live on the GPU or in pinned host memory")
+    _, Hkv, bs, D = src_k.shape
+    shape = make_shape(num_kv_heads=Hkv, head_dim=D, block_size=bs, num_blocks=src_k.shape[0],
+                       dtype=_DT[src_k.dtype])
+    _check("pkv_copy_blocks",
+           load_library().pkv_copy_blocks(ctypes.byref(shape), _ptr(src_k), _ptr(src_v),
+                                          src_k.shape[0], _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
+                                          _ptr(pairs), pairs.shape[0], _stream_ptr(stream)))
+
+
+class BlockManager:
+    """Host-side block manager of the C library (pkv_bm_* in include/pkv.h)."""
+
+    def __init__(self, num_gpu_blocks: int, num_cpu_blocks: int, block_size: int):
+        self._lib = load_library()
+        self._h = self._lib.pkv_bm_create(num_gpu_blocks, num_cpu_blocks, block_size)
+        if not self._h:
+            raise ValueError("bad block manager sizes")
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def _call(self, name, *args):
+        _check("pkv_bm_" + name, getattr(self._lib, "pkv_bm_" + name)(self._h, *args))
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> None:
+        self._call("add_sequence", seq_id, num_tokens)
+
+    def fork(self, parent: int, child: int) -> None:
+        self._call("fork", parent, child)
+
+    def append_token(self, seq_id: int) -> tuple[int, int, int]:
+        """(slot, copy_src, copy_dst); copy_* are -1 unless a shared block was copied."""
+        s, a, b = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        self._call("append_token", seq_id, ctypes.byref(s), ctypes.byref(a), ctypes.byref(b))
+        return s.value, a.value, b.value
+
+    def free_sequence(self, seq_id: int) -> None:
+        self._call("free_sequence", seq_id)
+
+    def _pairs(self, name, *args, cap=1 << 16):
+        import numpy as np
+        buf = (ctypes.c_int32 * (2 * cap))()
+        n = ctypes.c_int32()
+        self._call(name, *args, buf, cap, ctypes.byref(n))
+        return np.array(buf[: 2 * n.value], dtype=np.int32).reshape(-1, 2)
+
+    def swap_out(self, seq_id: int, gpu_window: int):
+        """(gpu id, cpu id) pairs [n, 2] of the blocks moved to the CPU pool."""
+        return self._pairs("swap_out", seq_id, gpu_window)
+
+    def swap_in(self, seq_id: int):
+        """(cpu id, gpu id) pairs [n, 2] of the blocks moved back to the GPU."""
+        return self._pairs("swap_in", seq_id)
+
+    def num_free(self) -> tuple[int, int]:
+        g, c = ctypes.c_int32(), ctypes.c_int32()
+        self._call("num_free", ctypes.byref(g), ctypes.byref(c))
+        return g.value, c.value
+
+    def seq_info(self, seq_id: int) -> tuple[int, int, int]:
+        a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        self._call("seq_info", seq_id, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+        return a.value, b.value, c.value
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int):
+        """(block_tables [n, MB] int32, context_lens [n] int32) as numpy arrays."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = ids.shape[0]
+        tables = np.zeros((n, max_blocks_per_seq), dtype=np.int32)
+        lens = np.zeros(n, dtype=np.int32)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        self._call("block_tables", ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+                   max_blocks_per_seq, tables.ctypes.data_as(i32p), lens.ctypes.data_as(i32p))
+        return tables, lens
 
 
 def get_device_error(stream=None) -> int:

@@ -52,6 +52,40 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ------------------------------------------------------------------ block copy
+// Whole-block copy between pools (copy-on-write within the GPU pool, swap-out
+// to and swap-in from a pinned CPU pool that the GPU reaches directly): pair
+// i copies block pairs[2i] of the source pool to block pairs[2i+1] of the
+// destination pool, every kv head, K and V.  CTA (i, K|V, part) moves up to
+// 16 KB with four independent 16-byte loads per thread before the stores.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                       uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                       const int32_t* __restrict__ pairs, int src_nb, int dst_nb,
+                       int chunks_per_block, int* err) {
+  const int pair = blockIdx.x >> 1;
+  const bool is_v = blockIdx.x & 1;
+  const int s = pairs[2 * pair], d = pairs[2 * pair + 1];
+  if (s < 0 || s >= src_nb || d < 0 || d >= dst_nb) {
+    if (threadIdx.x == 0 && !is_v && blockIdx.y == 0) record_error(err, kDevBadBlock);
+    return;
+  }
+  const uint4* src = (is_v ? src_v : src_k) + (size_t)s * chunks_per_block;
+  uint4* dst = (is_v ? dst_v : dst_k) + (size_t)d * chunks_per_block;
+  const int base = blockIdx.y * 1024 + threadIdx.x;
+  uint4 x[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = base + u * 256;
+    if (c < chunks_per_block) x[u] = src[c];
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = base + u * 256;
+    if (c < chunks_per_block) dst[c] = x[u];
+  }
+}
+
 // ------------------------------------------------------------------ reduce
 template <bool BF>
 cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
@@ -348,6 +382,7 @@ extern "C" const char* pkv_strerror(int code) {
     case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than pkv_workspace_bytes";
     case PKV_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case PKV_ERR_DEVICE: return "a kernel recorded a device-side error";
+    case PKV_ERR_NO_BLOCKS: return "the block pool has no free block left";
     default: return "unknown pkv error code";
   }
 }
@@ -511,6 +546,35 @@ extern "C" int pkv_decode_step(const pkv_shape* s, const void* q, const void* k_
   if (s->num_seqs > 0 && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_ALIGN;
   return decode_impl(s, q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
                      workspace_bytes, stream, k_new, v_new);
+}
+
+extern "C" int pkv_copy_blocks(const pkv_shape* s, const void* src_k, const void* src_v,
+                               int32_t src_num_blocks, void* dst_k, void* dst_v,
+                               int32_t dst_num_blocks, const int32_t* pairs, int32_t num_pairs,
+                               pkv_stream_t stream) {
+  if (!s) return PKV_ERR_NULL;
+  if (s->num_kv_heads < 1 || s->head_dim < 1 || s->block_size < 1 || src_num_blocks < 1 ||
+      dst_num_blocks < 1 || num_pairs < 0)
+    return PKV_ERR_INVALID;
+  if (s->dtype != PKV_F16 && s->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (s->head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!src_k || !src_v || !dst_k || !dst_v || !pairs) return PKV_ERR_NULL;
+  if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) || !aligned(dst_v, 16) ||
+      !aligned(pairs, 4))
+    return PKV_ERR_ALIGN;
+  const long long chunks = static_cast<long long>(s->num_kv_heads) * s->block_size * s->head_dim / 8;
+  if (chunks > (1ll << 30) || num_pairs > (1 << 30)) return PKV_ERR_UNSUPPORTED;
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  const dim3 grid(2u * static_cast<unsigned>(num_pairs), static_cast<unsigned>((chunks + 1023) / 1024));
+  copy_blocks_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v),
+      static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v), pairs, src_num_blocks,
+      dst_num_blocks, static_cast<int>(chunks), d->err);
+  g_launches.fetch_add(1);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 extern "C" int pkv_get_device_error(int32_t* code, pkv_stream_t stream) {

@@ -337,6 +337,19 @@ def check_append_then_decode_sees_token(lib):
     assert np.allclose(out[0, 0], _from_bits(_to_bits(vnew, dtype), dtype)[0, 0], atol=1e-12, rtol=0)
 
 
+def check_copy_blocks_matches_index_assignment(lib):
+    """Block copy equals numpy fancy-index assignment between pools of
+    different sizes; blocks not named as destinations stay unchanged."""
+    rng = np.random.default_rng(14)
+    src = rng.integers(0, 65536, size=(7, 2, 16, 64), dtype=np.uint16)
+    dst = rng.integers(0, 65536, size=(11, 2, 16, 64), dtype=np.uint16)
+    pairs = np.array([[3, 0], [6, 10], [0, 4], [3, 7]], dtype=np.int32)
+    got = oracle.copy_blocks(src, dst, pairs, lib)
+    exp = dst.copy()
+    exp[pairs[:, 1]] = src[pairs[:, 0]]
+    assert np.array_equal(got, exp)
+
+
 ALL_CHECKS = [
     check_half_decode_exhaustive,
     check_bf16_decode_exhaustive,
@@ -353,4 +366,5 @@ ALL_CHECKS = [
     check_scale_enters_logits,
     check_append_matches_index_assignment,
     check_append_then_decode_sees_token,
+    check_copy_blocks_matches_index_assignment,
 ]

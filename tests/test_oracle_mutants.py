@@ -32,6 +32,8 @@ MUTANTS = {
     "append_offset": ("int blk = s / bs, off = s % bs;", "int blk = s / bs, off = s % bs ^ 1;"),
     "append_negative_slot_written": ("if (s < 0) continue;", "if (s < 0) s = 0;"),
     "q_head_shared": ("q + ((size_t)i * Hq + h) * D;", "q + ((size_t)i * Hq + h / (Hq / Hkv)) * D;"),
+    "copy_swapped_pair": ("int s = pairs[2 * i], d = pairs[2 * i + 1];",
+                          "int d = pairs[2 * i], s = pairs[2 * i + 1];"),
 }
 
 
