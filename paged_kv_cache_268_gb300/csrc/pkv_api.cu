@@ -87,50 +87,65 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ reduce
+// Launch a dependent kernel with programmatic stream serialisation: it may
+// start launching while the decode kernel's last CTAs still run, and waits
+// (griddepcontrol.wait) for that grid before reading its partials.
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 template <bool BF>
 cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
-  const int rows = a.B * a.Hq;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  const unsigned grid = static_cast<unsigned>((a.B * a.Hq + 7) / 8);
+  const float* po = a.part_o;
+  const float2* pml = a.part_ml;
+  const int32_t* cl = a.context_lens;
   switch (D) {
     case 64:
-      split_reduce_kernel<BF, 64><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.context_lens,
-                                                           a.out, a.B, a.Hq, a.S, a.P, a.max_ctx);
-      break;
+      return launch_dependent(split_reduce_kernel<BF, 64>, grid, stream, po, pml, cl, a.out, a.B,
+                              a.Hq, a.S, a.P, a.max_ctx);
     case 128:
-      split_reduce_kernel<BF, 128><<<grid, 256, 0, stream>>>(
-          a.part_o, a.part_ml, a.context_lens, a.out, a.B, a.Hq, a.S, a.P, a.max_ctx);
-      break;
+      return launch_dependent(split_reduce_kernel<BF, 128>, grid, stream, po, pml, cl, a.out, a.B,
+                              a.Hq, a.S, a.P, a.max_ctx);
     case 256:
-      split_reduce_kernel<BF, 256><<<grid, 256, 0, stream>>>(
-          a.part_o, a.part_ml, a.context_lens, a.out, a.B, a.Hq, a.S, a.P, a.max_ctx);
-      break;
+      return launch_dependent(split_reduce_kernel<BF, 256>, grid, stream, po, pml, cl, a.out, a.B,
+                              a.Hq, a.S, a.P, a.max_ctx);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <bool BF>
 cudaError_t launch_merge(const DecodeArgs& a, int D, cudaStream_t stream) {
-  const int rows = a.B * a.Hq;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  const unsigned grid = static_cast<unsigned>((a.B * a.Hq + 7) / 8);
+  const float* po = a.part_o;
+  const float2* pml = a.part_ml;
+  const int* hdr = a.hdr;
   switch (D) {
     case 64:
-      persistent_merge_kernel<BF, 64><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.hdr, a.out,
-                                                               a.B, a.Hq, a.Hkv);
-      break;
+      return launch_dependent(persistent_merge_kernel<BF, 64>, grid, stream, po, pml, hdr, a.out,
+                              a.B, a.Hq, a.Hkv);
     case 128:
-      persistent_merge_kernel<BF, 128><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.hdr,
-                                                                a.out, a.B, a.Hq, a.Hkv);
-      break;
+      return launch_dependent(persistent_merge_kernel<BF, 128>, grid, stream, po, pml, hdr, a.out,
+                              a.B, a.Hq, a.Hkv);
     case 256:
-      persistent_merge_kernel<BF, 256><<<grid, 256, 0, stream>>>(a.part_o, a.part_ml, a.hdr,
-                                                                a.out, a.B, a.Hq, a.Hkv);
-      break;
+      return launch_dependent(persistent_merge_kernel<BF, 256>, grid, stream, po, pml, hdr, a.out,
+                              a.B, a.Hq, a.Hkv);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // Persistent schedule: phase-1 CTAs (two per SM, resident from the start) and

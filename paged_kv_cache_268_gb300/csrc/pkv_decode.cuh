@@ -428,6 +428,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   int* ids = reinterpret_cast<int*>(bars + NW * NS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The reduce kernel may start launching once every CTA of this grid has
+  // started; it waits for this grid's completion before reading partials.
+  pdl_launch_dependents();
   int idx = blockIdx.x;
   const int split = idx % a.S;
   idx /= a.S;
@@ -685,6 +688,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B, Hkv = a.Hkv;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -847,6 +851,7 @@ __global__ void __launch_bounds__(256)
                             const int* __restrict__ hdr, uint16_t* __restrict__ out, int B,
                             int Hq, int Hkv) {
   constexpr int OPL = D / 32;
+  pdl_wait();
   const int gq = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gq >= B * Hq) return;
@@ -904,6 +909,7 @@ __global__ void __launch_bounds__(256)
                         const int32_t* __restrict__ context_lens, uint16_t* __restrict__ out,
                         int B, int Hq, int S, int P, int max_ctx) {
   constexpr int OPL = D / 32;
+  pdl_wait();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= B * Hq) return;

@@ -169,6 +169,14 @@ __device__ __forceinline__ uint16_t to_elem(float x) {
   }
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// launching, and, in that kernel, wait until the previous grid has finished
+// and its memory is visible (a no-op for ordinary launches).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void record_error(int* err, int code) {
   atomicCAS(err, 0, code);
 }
