@@ -72,7 +72,8 @@ enum {
  *   num_seqs            B, sequences in the batch (one query token each)
  *   num_q_heads         Hq
  *   num_kv_heads        Hkv; Hq % Hkv == 0; query head h reads kv head
- *                       h / (Hq / Hkv) (contiguous grouping)
+ *                       h / (Hq / Hkv) (contiguous grouping); the group
+ *                       size Hq / Hkv is at most 32
  *   head_dim            D, one of 64, 128, 256
  *   block_size          bs, tokens per physical block, one of 16, 32
  *   num_blocks          NB, physical blocks in the pool
@@ -111,7 +112,8 @@ typedef struct {
   int32_t schedule;
   int32_t split_tokens;     /* P, tokens per partition (schedule 0; else 0) */
   int32_t num_splits;       /* S = ceil(max_context_len / P) (schedule 0; else 0) */
-  int32_t variant;          /* 0 = CUDA-core kernel, 1 = tensor-core (mma) kernel */
+  int32_t variant;          /* 0 = CUDA-core kernel (group 1-2), 1 = tensor-core
+                               mma kernel (group 3-32) */
   int32_t warps_per_cta;
   int32_t stages_per_warp;
   int32_t grid_ctas;

@@ -297,7 +297,7 @@ int check_decode_shape(const pkv_shape* s) {
       static_cast<long long>(s->max_blocks_per_seq) * s->block_size)
     return PKV_ERR_INVALID;
   const int G = s->num_q_heads / s->num_kv_heads;
-  if (G > 8) return PKV_ERR_UNSUPPORTED;
+  if (G > 32) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
 }
 

@@ -234,27 +234,31 @@ struct SimtCompute {
 };
 
 // ------------------------------------------------------------------ MMA
-template <bool BF, int D, int BS>
+// NT n-tiles of 8 query heads each (group sizes up to 8 * NT).
+template <bool BF, int D, int BS, int NT = 1>
 struct MmaCompute {
   static constexpr int KS = D / 16;    // k-steps of QK, d-tiles of PV
   static constexpr int MT = BS / 16;   // 16-token m-tiles per block
-  static constexpr int NH = 8;         // heads this warp produces (N of the tile)
+  static constexpr int NH = 8 * NT;    // heads this warp produces (N of the tiles)
 
-  uint32_t qf[KS][2];                  // Q^T B-fragments
-  float o[KS][4];                      // O^T accumulators
-  float m[2], l[2];                    // heads 2*(lane%4) + {0, 1}
+  uint32_t qf[KS][NT][2];              // Q^T B-fragments
+  float o[KS][NT][4];                  // O^T accumulators
+  float m[NT][2], l[NT][2];            // heads nt*8 + 2*(lane%4) + {0, 1}
 
   // q rows of the group start at `qg` (G rows of D elements); lane holds the
-  // Q^T B-fragments of head lane / 4 (zero for the padding heads >= G).
+  // Q^T B-fragments of heads nt*8 + lane/4 (zero for the padding heads >= G).
   __device__ __forceinline__ void load_q(const uint16_t* qg, int G, int lane) {
-    const int h = lane >> 2;
     const int c = 2 * (lane & 3);
-    const bool real = h < G;
-    const uint16_t* qrow = qg + (real ? h : 0) * D;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qf[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + c) : 0u;
-      qf[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + c) : 0u;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + (lane >> 2);
+      const bool real = h < G;
+      const uint16_t* qrow = qg + (real ? h : 0) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][nt][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + c) : 0u;
+        qf[ks][nt][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + c) : 0u;
+      }
     }
   }
 
@@ -262,93 +266,73 @@ struct MmaCompute {
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[ks][e] = 0.f;
-    m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
-  }
-
-  // As SimtCompute::finish, for the G real heads of the tile.
-  __device__ __forceinline__ void finish(bool final_rows, uint16_t* out_rows, float* po,
-                                         float2* pml, int G, int lane) {
-    float lt[2];
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float v = l[j];
-      v += __shfl_xor_sync(kFull, v, 4);
-      v += __shfl_xor_sync(kFull, v, 8);
-      v += __shfl_xor_sync(kFull, v, 16);
-      lt[j] = v;
-    }
+        for (int e = 0; e < 4; ++e) o[ks][nt][e] = 0.f;
 #pragma unroll
-    for (int dt = 0; dt < KS; ++dt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = dt * 16 + (lane >> 2) + ((e >> 1) << 3);
-        const int h = 2 * (lane & 3) + (e & 1);
-        if (h < G) {
-          if (final_rows)
-            out_rows[h * D + d] = to_elem<BF>(o[dt][e] / lt[e & 1]);
-          else
-            po[h * D + d] = o[dt][e];
-        }
-      }
-    if (!final_rows && lane < 4) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        if (2 * lane + j < G) pml[2 * lane + j] = make_float2(m[j], lt[j]);
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
     }
   }
 
   __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float scale_log2,
                                         int lane) {
-    float s[MT][4];
+    float s[MT][NT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[mt][e] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[mt][nt][e] = 0.f;
       const int r = mt * 16 + (lane & 15);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(kt + tile_off<BS>(r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-        mma_16816<BF>(s[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816<BF>(s[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
       }
     }
     // logits in log2 units; rows past the context end are masked
-    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int nt = 0; nt < NT; ++nt) {
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = mt * 16 + (lane >> 2) + ((e >> 1) << 3);
-        const float x = (tok < valid) ? s[mt][e] * scale_log2 : -INFINITY;
-        s[mt][e] = x;
-        mx[e & 1] = fmaxf(mx[e & 1], x);
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = mt * 16 + (lane >> 2) + ((e >> 1) << 3);
+          const float x = (tok < valid) ? s[mt][nt][e] * scale_log2 : -INFINITY;
+          s[mt][nt][e] = x;
+          mx[e & 1] = fmaxf(mx[e & 1], x);
+        }
+      float alpha[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float v = mx[j];
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, 16));
+        const float mn = fmaxf(m[nt][j], v);
+        alpha[j] = fast_exp2(m[nt][j] - mn);
+        m[nt][j] = mn;
+        l[nt][j] *= alpha[j];
       }
-    float alpha[2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float v = mx[j];
-      v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(kFull, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(kFull, v, 16));
-      const float mn = fmaxf(m[j], v);
-      alpha[j] = fast_exp2(m[j] - mn);
-      m[j] = mn;
-      l[j] *= alpha[j];
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pe = fast_exp2(s[mt][nt][e] - m[nt][e & 1]);
+          s[mt][nt][e] = pe;
+          l[nt][e & 1] += pe;
+        }
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[dt][nt][e] *= alpha[e & 1];
     }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pe = fast_exp2(s[mt][e] - m[e & 1]);
-        s[mt][e] = pe;
-        l[e & 1] += pe;
-      }
-#pragma unroll
-    for (int dt = 0; dt < KS; ++dt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[dt][e] *= alpha[e & 1];
 
     if (valid < BS) {
       // Rows past the context end carry whatever the block held; P is 0 there,
@@ -369,44 +353,89 @@ struct MmaCompute {
       // P^T as the B operand.  bfloat16 keeps only 8 significant bits, so P
       // is carried as hi + lo (both bfloat16, ~16 bits together) and
       // multiplied twice; binary16's 11 bits are enough on their own.
-      const uint32_t h0 = pack2<BF>(s[mt][0], s[mt][1]);
-      const uint32_t h1 = pack2<BF>(s[mt][2], s[mt][3]);
-      const uint32_t b0 = movmatrix_trans(h0);
-      const uint32_t b1 = movmatrix_trans(h1);
-      uint32_t c0 = 0, c1 = 0;
-      if constexpr (BF) {
-        const float2 f0 = unpack2<BF>(h0), f1 = unpack2<BF>(h1);
-        c0 = movmatrix_trans(pack2<BF>(s[mt][0] - f0.x, s[mt][1] - f0.y));
-        c1 = movmatrix_trans(pack2<BF>(s[mt][2] - f1.x, s[mt][3] - f1.y));
+      uint32_t b0[NT], b1[NT], c0[NT], c1[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t h0 = pack2<BF>(s[mt][nt][0], s[mt][nt][1]);
+        const uint32_t h1 = pack2<BF>(s[mt][nt][2], s[mt][nt][3]);
+        b0[nt] = movmatrix_trans(h0);
+        b1[nt] = movmatrix_trans(h1);
+        c0[nt] = c1[nt] = 0;
+        if constexpr (BF) {
+          const float2 f0 = unpack2<BF>(h0), f1 = unpack2<BF>(h1);
+          c0[nt] = movmatrix_trans(pack2<BF>(s[mt][nt][0] - f0.x, s[mt][nt][1] - f0.y));
+          c1[nt] = movmatrix_trans(pack2<BF>(s[mt][nt][2] - f1.x, s[mt][nt][3] - f1.y));
+        }
       }
       const int r = mt * 16 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
       for (int dt = 0; dt < KS; ++dt) {
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(vt + tile_off<BS>(r, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
-        mma_16816<BF>(o[dt], a0, a1, a2, a3, b0, b1);
-        if constexpr (BF) mma_16816<BF>(o[dt], a0, a1, a2, a3, c0, c1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_16816<BF>(o[dt][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+          if constexpr (BF) mma_16816<BF>(o[dt][nt], a0, a1, a2, a3, c0[nt], c1[nt]);
+        }
       }
     }
   }
 
   __device__ __forceinline__ void publish(float* cm, float* cl, float* co, int lane) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float lt = l[j];
-      lt += __shfl_xor_sync(kFull, lt, 4);
-      lt += __shfl_xor_sync(kFull, lt, 8);
-      lt += __shfl_xor_sync(kFull, lt, 16);
-      if (lane < 4) { cm[2 * lane + j] = m[j]; cl[2 * lane + j] = lt; }
-    }
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-    for (int dt = 0; dt < KS; ++dt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = dt * 16 + (lane >> 2) + ((e >> 1) << 3);
-        const int h = 2 * (lane & 3) + (e & 1);
-        co[h * D + d] = o[dt][e];
+      for (int j = 0; j < 2; ++j) {
+        float lt = l[nt][j];
+        lt += __shfl_xor_sync(kFull, lt, 4);
+        lt += __shfl_xor_sync(kFull, lt, 8);
+        lt += __shfl_xor_sync(kFull, lt, 16);
+        if (lane < 4) { cm[nt * 8 + 2 * lane + j] = m[nt][j]; cl[nt * 8 + 2 * lane + j] = lt; }
       }
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = dt * 16 + (lane >> 2) + ((e >> 1) << 3);
+          const int h = nt * 8 + 2 * (lane & 3) + (e & 1);
+          co[h * D + d] = o[dt][nt][e];
+        }
+    }
+  }
+
+  // As SimtCompute::finish, for the G real heads of the tiles.
+  __device__ __forceinline__ void finish(bool final_rows, uint16_t* out_rows, float* po,
+                                         float2* pml, int G, int lane) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float lt[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float v = l[nt][j];
+        v += __shfl_xor_sync(kFull, v, 4);
+        v += __shfl_xor_sync(kFull, v, 8);
+        v += __shfl_xor_sync(kFull, v, 16);
+        lt[j] = v;
+      }
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = dt * 16 + (lane >> 2) + ((e >> 1) << 3);
+          const int h = nt * 8 + 2 * (lane & 3) + (e & 1);
+          if (h < G) {
+            if (final_rows)
+              out_rows[h * D + d] = to_elem<BF>(o[dt][nt][e] / lt[e & 1]);
+            else
+              po[h * D + d] = o[dt][nt][e];
+          }
+        }
+      if (!final_rows && lane < 4) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          if (nt * 8 + 2 * lane + j < G) pml[nt * 8 + 2 * lane + j] = make_float2(m[nt][j], lt[j]);
+      }
+    }
   }
 };
 
@@ -420,11 +449,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
   constexpr int STAGE = 2 * TILE;
   constexpr int CH = D / 64;
   constexpr int NH = Compute::NH;
+  // The warps' final (m, l, o) merge reuses the ring; barriers and block ids
+  // sit after whichever of the two is larger.
+  constexpr int RING = NW * NS * STAGE;
+  constexpr int MERGE = NW * NH * (D + 2) * 4;
+  constexpr int TAIL = ((RING > MERGE ? RING : MERGE) + 15) & ~15;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NS * STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TAIL);
   int* ids = reinterpret_cast<int*>(bars + NW * NS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -544,7 +578,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   cs.publish(cm + warp * NH, cl + warp * NH, co + warp * NH * D, lane);
   __syncthreads();
 
-  const int nh = (NH == 8) ? a.G : NH;
+  const int nh = a.G;  // heads of this kv head's group (<= NH)
   const bool single = (L + a.P - 1) / a.P == 1;
   for (int i = threadIdx.x; i < nh * D; i += NW * 32) {
     const int h = i / D, d = i - h * D;

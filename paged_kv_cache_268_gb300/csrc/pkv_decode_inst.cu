@@ -44,9 +44,10 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
     kern<<<grid, NW * 32, geo_persist_smem(D, BS, a.B), stream>>>(a, tk, tv);
     return cudaGetLastError();
   }
-  constexpr int SMEM = geo_smem(D, BS);
-  static_assert(NW * Compute::NH * (D + 2) * 4 <= NW * NS * stage_bytes(D, BS),
-                "merge area must fit in the stage ring");
+  // the warps' (m, l, o) merge reuses the stage ring; wide groups need more
+  constexpr int RING = NW * NS * stage_bytes(D, BS);
+  constexpr int MERGE = NW * Compute::NH * (D + 2) * 4;
+  constexpr int SMEM = geo_smem(D, BS) + (MERGE > RING ? ((MERGE - RING + 15) & ~15) : 0);
   auto kern = paged_decode_kernel<kBF, D, BS, NW, NS, Compute>;
   static int mask = 0;
   cudaError_t e = configure(kern, SMEM, &mask);
@@ -61,7 +62,11 @@ cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& tk, const CUt
                            int schedule, int grid, cudaStream_t stream) {
 #if PKV_INST_MMA
   if (a.G >= 3 && a.G <= 8)
-    return launch_one<D, BS, MmaCompute<kBF, D, BS>>(a, tk, tv, schedule, grid, stream);
+    return launch_one<D, BS, MmaCompute<kBF, D, BS, 1>>(a, tk, tv, schedule, grid, stream);
+  if (a.G >= 9 && a.G <= 16)
+    return launch_one<D, BS, MmaCompute<kBF, D, BS, 2>>(a, tk, tv, schedule, grid, stream);
+  if (a.G >= 17 && a.G <= 32)
+    return launch_one<D, BS, MmaCompute<kBF, D, BS, 4>>(a, tk, tv, schedule, grid, stream);
 #else
   if (a.G == 1)
     return launch_one<D, BS, SimtCompute<kBF, D, BS, 1>>(a, tk, tv, schedule, grid, stream);

@@ -56,7 +56,7 @@ def _decode(lib, shape, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE, ws
     (dict(head_dim=96), -3),
     (dict(block_size=8), -3),
     (dict(dtype=5), -3),
-    (dict(num_q_heads=32, num_kv_heads=2), -3),          # group of 16 not built
+    (dict(num_q_heads=66, num_kv_heads=2), -3),          # group of 33 not built
     (dict(num_blocks=1 << 24, num_kv_heads=8, num_q_heads=8), -3),  # rows overflow int32
 ])
 def test_decode_rejects_bad_shapes(lib, kw, code):

@@ -78,7 +78,7 @@ def test_split_count_invariance(pkv, split):
 
 
 @pytest.mark.parametrize("dtype", [W.F16, W.BF16])
-@pytest.mark.parametrize("G", [1, 2, 3, 4, 6, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 6, 8, 12, 16, 24, 32])
 @pytest.mark.parametrize("D,bs", [(64, 16), (128, 16), (128, 32), (256, 16), (64, 32), (256, 32)])
 def test_shape_sweep(pkv, dtype, G, D, bs):
     Hkv = 2
