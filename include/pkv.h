@@ -83,8 +83,17 @@ enum {
  *   dtype               pkv_dtype
  *   split_tokens        schedule choice: 0 lets the library choose the
  *                       partition size; > 0 sets the tokens per split-KV
- *                       partition (rounded up to a multiple of bs); -1 selects
- *                       the persistent schedule (num_seqs <= 2048) */
+ *                       partition (rounded up to a multiple of bs, and of 128
+ *                       for the tcgen05 kernel); -1 selects the persistent
+ *                       schedule (num_seqs <= 2048)
+ *   kernel              inner-loop choice: 0 lets the library choose, 1 CUDA
+ *                       cores (group size 1-2), 2 mma.sync tensor cores
+ *                       (group 3-32), 3 tcgen05 tensor cores with TMEM
+ *                       accumulators (head_dim 128, group 1-32, partition
+ *                       schedule; decode only).  The library's choice: 1 for
+ *                       groups of 1-2, 2 for 3-8, 3 for 9-32 at head_dim 128
+ *                       (2 otherwise).  An inapplicable choice gives
+ *                       PKV_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -96,6 +105,7 @@ typedef struct {
   int32_t max_context_len;
   int32_t dtype;
   int32_t split_tokens;
+  int32_t kernel;
 } pkv_shape;
 
 /* How a decode call will run (filled by pkv_decode_plan).
@@ -112,8 +122,8 @@ typedef struct {
   int32_t schedule;
   int32_t split_tokens;     /* P, tokens per partition (schedule 0; else 0) */
   int32_t num_splits;       /* S = ceil(max_context_len / P) (schedule 0; else 0) */
-  int32_t variant;          /* 0 = CUDA-core kernel (group 1-2), 1 = tensor-core
-                               mma kernel (group 3-32) */
+  int32_t variant;          /* 0 = CUDA-core kernel, 1 = mma.sync tensor-core
+                               kernel, 2 = tcgen05 tensor-core kernel */
   int32_t warps_per_cta;
   int32_t stages_per_warp;
   int32_t grid_ctas;

@@ -32,7 +32,7 @@ class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "block_size",
         "num_blocks", "max_blocks_per_seq", "max_context_len", "dtype",
-        "split_tokens")]
+        "split_tokens", "kernel")]
 
 
 class Plan(ctypes.Structure):
@@ -133,9 +133,9 @@ def _check(fn: str, rc: int):
 
 def make_shape(*, num_seqs=0, num_q_heads=1, num_kv_heads=1, head_dim=128, block_size=16,
                num_blocks=1, max_blocks_per_seq=1, max_context_len=1, dtype=PKV_F16,
-               split_tokens=0) -> Shape:
+               split_tokens=0, kernel=0) -> Shape:
     return Shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                 max_blocks_per_seq, max_context_len, dtype, split_tokens)
+                 max_blocks_per_seq, max_context_len, dtype, split_tokens, kernel)
 
 
 def _cache_shape(k_cache: torch.Tensor) -> tuple[int, int, int, int]:
@@ -172,7 +172,8 @@ def kv_cache_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor
 
 
 def decode_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
-                 max_context_len: int | None = None, split_tokens: int = 0) -> Shape:
+                 max_context_len: int | None = None, split_tokens: int = 0,
+                 kernel: int = 0) -> Shape:
     NB, Hkv, bs, D = _cache_shape(k_cache)
     B, Hq, Dq = q.shape
     MB = block_tables.shape[1]
@@ -180,7 +181,7 @@ def decode_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Ten
         max_context_len = MB * bs        # always a valid bound; needs no host sync
     return make_shape(num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
                       num_blocks=NB, max_blocks_per_seq=MB, max_context_len=int(max_context_len),
-                      dtype=_DT[q.dtype], split_tokens=int(split_tokens))
+                      dtype=_DT[q.dtype], split_tokens=int(split_tokens), kernel=int(kernel))
 
 
 def decode_plan(shape: Shape) -> Plan:
@@ -205,14 +206,15 @@ def alloc_workspace(shape: Shape, device=None) -> torch.Tensor | None:
 def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                       out: torch.Tensor | None = None, *, max_context_len: int | None = None,
-                      split_tokens: int = 0, workspace: torch.Tensor | None = None,
+                      split_tokens: int = 0, kernel: int = 0,
+                      workspace: torch.Tensor | None = None,
                       stream=None) -> torch.Tensor:
     """softmax(q . K^T * scale) . V per (sequence, query head) over the paged cache.
 
     q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables [B, MB] int32;
     context_lens [B] int32.  Returns out [B, Hq, D] (allocated if not given).
     split_tokens: 0 = library's choice, > 0 = partition size, -1 = persistent
-    schedule.
+    schedule.  kernel: 0 = library's choice, 1 CUDA cores, 2 mma.sync, 3 tcgen05.
     """
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _dense(t, n, q.dtype)
@@ -226,7 +228,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         out = torch.empty_like(q)
     else:
         _dense(out, "out", q.dtype)
-    shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens)
+    shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens, kernel)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
     lib = load_library()

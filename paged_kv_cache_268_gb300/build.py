@@ -33,7 +33,7 @@ def nvcc() -> str:
 
 def _units():
     units = [("pkv_api", "pkv_api.cu", []), ("pkv_noalloc", "pkv_noalloc.cu", []),
-             ("pkv_blocks", "pkv_blocks.cpp", [])]
+             ("pkv_blocks", "pkv_blocks.cpp", []), ("pkv_decode_tc", "pkv_decode_tc.cu", [])]
     for bf in (0, 1):
         for mma in (0, 1):
             name = f"pkv_decode_{'bf16' if bf else 'f16'}_{'mma' if mma else 'simt'}"

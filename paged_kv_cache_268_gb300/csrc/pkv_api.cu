@@ -290,7 +290,7 @@ int check_decode_shape(const pkv_shape* s) {
   int rc = check_cache_shape(s);
   if (rc != PKV_OK) return rc;
   if (s->num_seqs < 0 || s->num_q_heads < 1 || s->max_blocks_per_seq < 1 ||
-      s->max_context_len < 1 || s->split_tokens < -1)
+      s->max_context_len < 1 || s->split_tokens < -1 || s->kernel < 0 || s->kernel > 3)
     return PKV_ERR_INVALID;
   if (s->num_q_heads % s->num_kv_heads != 0) return PKV_ERR_INVALID;
   if (static_cast<long long>(s->max_context_len) >
@@ -301,12 +301,35 @@ int check_decode_shape(const pkv_shape* s) {
   return PKV_OK;
 }
 
-int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
+// Inner-loop variant (0 CUDA cores, 1 mma.sync, 2 tcgen05) for a shape, or -1
+// when the requested one cannot run it.  The tcgen05 kernel serves the
+// partition schedule of a plain decode only.
+int pick_variant(const pkv_shape* s, bool fused) {
+  const int G = s->num_q_heads / s->num_kv_heads;
+  const bool tc_ok = s->head_dim == 128 && G <= 32 && s->split_tokens != -1 && !fused;
+  switch (s->kernel) {
+    case 1: return G <= 2 ? 0 : -1;
+    case 2: return 1;
+    case 3: return tc_ok ? 2 : -1;
+    default:
+      if (G <= 2) return 0;
+      if (G <= 8) return 1;
+      return tc_ok ? 2 : 1;
+  }
+}
+
+int make_plan(const pkv_shape* s, int sms, pkv_plan* plan, bool fused = false) {
   const int G = s->num_q_heads / s->num_kv_heads;
   const int bs = s->block_size;
-  plan->variant = G <= 2 ? 0 : 1;
+  plan->variant = pick_variant(s, fused);
+  if (plan->variant < 0) return PKV_ERR_UNSUPPORTED;
   KernelGeometry geo{};
   decode_geometry(s->head_dim, bs, plan->variant, &geo);
+  if (plan->variant == 2) {
+    geo.warps = 4;
+    geo.stages = 3;   // tile slots of 128 tokens
+    geo.smem_bytes = tc_smem_bytes(G);
+  }
   plan->warps_per_cta = geo.warps;
   plan->stages_per_warp = geo.stages;
   const long long units = static_cast<long long>(s->num_seqs) * s->num_kv_heads;
@@ -327,7 +350,8 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   }
   plan->schedule = 0;
   const int maxL = s->max_context_len;
-  const int gran = bs * geo.warps;           // every warp gets the same block count
+  // every warp gets the same block count; the tcgen05 kernel walks 128-token groups
+  const int gran = plan->variant == 2 ? 128 : bs * geo.warps;
   const int cap = kMaxBlocksPerCta * bs;      // ids of one partition fit in shared memory
   long long P;
   if (s->split_tokens > 0) {
@@ -464,7 +488,7 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   rc = current_device(&d);
   if (rc != PKV_OK) return rc;
   pkv_plan plan{};
-  rc = make_plan(s, d->sms, &plan);
+  rc = make_plan(s, d->sms, &plan, k_new != nullptr);
   if (rc != PKV_OK) return rc;
   if (k_new && plan.schedule != 0) return PKV_ERR_UNSUPPORTED;
   if (plan.workspace_bytes > 0) {
@@ -520,7 +544,9 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   const bool bf = s->dtype == PKV_BF16;
   const int D = s->head_dim, BS = s->block_size, sc = plan.schedule, grid = plan.grid_ctas;
   cudaError_t e;
-  if (plan.variant == 0)
+  if (plan.variant == 2)
+    e = launch_decode_tc(a, tk, tv, bf, D, BS, st);
+  else if (plan.variant == 0)
     e = bf ? launch_decode_bf16_simt(a, tk, tv, D, BS, sc, grid, st)
            : launch_decode_f16_simt(a, tk, tv, D, BS, sc, grid, st);
   else

@@ -61,7 +61,7 @@ template <int D, int BS>
 cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                            int schedule, int grid, cudaStream_t stream) {
 #if PKV_INST_MMA
-  if (a.G >= 3 && a.G <= 8)
+  if (a.G >= 1 && a.G <= 8)
     return launch_one<D, BS, MmaCompute<kBF, D, BS, 1>>(a, tk, tv, schedule, grid, stream);
   if (a.G >= 9 && a.G <= 16)
     return launch_one<D, BS, MmaCompute<kBF, D, BS, 2>>(a, tk, tv, schedule, grid, stream);

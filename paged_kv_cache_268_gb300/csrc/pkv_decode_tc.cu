@@ -1,0 +1,50 @@
+// Instantiates the tcgen05 decode kernel (head_dim 128; block size 16 or 32;
+// N = 16 or 32 padded query heads; binary16 or bfloat16).
+#include "pkv_decode_tc.cuh"
+
+namespace pkv {
+namespace {
+
+template <bool BF, int BS, int N>
+cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                      cudaStream_t stream) {
+  constexpr int SMEM = TcLayout<N>::BYTES;
+  static_assert(SMEM <= 227 * 1024, "tcgen05 kernel shared memory");
+  auto kern = paged_decode_tc<BF, BS, N>;
+  static int mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 32 && !(mask & (1 << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    mask |= 1 << dev;
+  }
+  const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * a.S;
+  kern<<<grid, 128, SMEM, stream>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+template <bool BF>
+cudaError_t dispatch_tc(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                        int block_size, cudaStream_t stream) {
+  const bool wide = a.G > 16;
+  if (block_size == 16)
+    return wide ? launch_tc<BF, 16, 32>(a, tk, tv, stream) : launch_tc<BF, 16, 16>(a, tk, tv, stream);
+  if (block_size == 32)
+    return wide ? launch_tc<BF, 32, 32>(a, tk, tv, stream) : launch_tc<BF, 32, 16>(a, tk, tv, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                             bool bf16, int head_dim, int block_size, cudaStream_t stream) {
+  if (head_dim != 128 || a.G < 1 || a.G > 32) return cudaErrorInvalidValue;
+  return bf16 ? dispatch_tc<true>(a, tk, tv, block_size, stream)
+              : dispatch_tc<false>(a, tk, tv, block_size, stream);
+}
+
+int tc_smem_bytes(int G) { return G > 16 ? TcLayout<32>::BYTES : TcLayout<16>::BYTES; }
+
+}  // namespace pkv

@@ -46,8 +46,8 @@ struct KernelGeometry {
   int smem_bytes;   // dynamic shared memory per CTA
 };
 
-// Variant: 0 = CUDA-core kernel (group size 1 or 2), 1 = tensor-core kernel
-// (group size 3..8).
+// Variant: 0 = CUDA-core kernel (group size 1 or 2), 1 = mma.sync tensor-core
+// kernel (group size 1..32), 2 = tcgen05 kernel (its geometry is its own).
 bool decode_geometry(int head_dim, int block_size, int variant, KernelGeometry* g);
 
 // Launch the decode kernel.  schedule 0: fixed partitions, grid B * Hkv * S;
@@ -65,6 +65,12 @@ cudaError_t launch_decode_f16_mma(const DecodeArgs&, const CUtensorMap&, const C
 cudaError_t launch_decode_bf16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
                                    int head_dim, int block_size, int schedule, int grid,
                                    cudaStream_t);
+
+// tcgen05 variant (head_dim 128, group size up to 32): same grid as the
+// partition schedule, partitions a multiple of 128 tokens.
+cudaError_t launch_decode_tc(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&, bool bf16,
+                             int head_dim, int block_size, cudaStream_t);
+int tc_smem_bytes(int group_size);
 
 int* device_error_word();  // device address of the error word (current device)
 

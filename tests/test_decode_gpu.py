@@ -199,3 +199,41 @@ def test_full_size_sampled(pkv, name):
         out = widen_out(gpu_decode(pkv, w, d, split_tokens=split))
         assert np.all(np.isfinite(out))
         assert_close(out[rows[:, 0], rows[:, 1]], ref, f"{name} split={split}")
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("G", [1, 4, 8, 12, 16, 24, 32])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_tcgen05_kernel(pkv, dtype, G, bs):
+    """The tcgen05/TMEM kernel (kernel=3) on ragged lengths spanning several
+    128-token groups and partitions."""
+    Hkv = 2
+    spec = W.WorkloadSpec("tc", 6, G * Hkv, Hkv, 128, bs, dtype, 0, 0, "uniform", (1, 1))
+    lens = np.array([1, 127, 128, 129, 700, 1500], dtype=np.int32)
+    spec = W.scaled(spec, 6, int(lens.max()))
+    w = W.make(spec, seed=G * 7 + bs, lens=lens)
+    d = device_inputs(w)
+    plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
+                                            w.max_context_len, 0, 3))
+    assert plan.variant == 2 and plan.schedule == 0
+    ref = oracle_decode(w)
+    for split in (0, 256, 1 << 20):
+        out = pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                    d["context_lens"], w.scale, max_context_len=w.max_context_len,
+                                    split_tokens=split, kernel=3)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert_close(widen_out(out), ref, f"tcgen05 G={G} bs={bs} split={split}")
+
+
+def test_kernel_choice_rules(pkv):
+    w = W.make(W.scaled(W.WORKLOADS["llama3_8b_gqa"], 2, 64), seed=0)
+    d = device_inputs(w)
+    shp = lambda k, split=0: pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
+                                              w.max_context_len, split, k)
+    assert pkv.decode_plan(shp(0)).variant == 1          # group 4 -> mma.sync
+    assert pkv.decode_plan(shp(3)).variant == 2
+    with pytest.raises(pkv.PkvError):
+        pkv.decode_plan(shp(1))                          # CUDA cores need group <= 2
+    with pytest.raises(pkv.PkvError):
+        pkv.decode_plan(shp(3, -1))                      # tcgen05 has no persistent schedule
