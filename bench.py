@@ -52,7 +52,10 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.ORDER)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
+    p.add_argument("--kernel", type=int, default=0,
+                   help="inner loop: 0 library's choice, 1 CUDA cores, 2 mma.sync, 3 tcgen05 "
+                        "(tcgen05 runs the two-call step)")
     p.add_argument("--num-seqs", type=int, default=0,
                    help="shrink the batch (and pool) for profiler captures; 0 = full workload")
     p.add_argument("--seed", type=int, default=0)
@@ -346,7 +349,9 @@ def run_pkv(args):
     k_new, v_new = w.k_new, w.v_new
     out = torch.empty_like(q)
     maxL = w.max_context_len
-    shape = pkv.decode_shape(q, kc, bt, maxL, args.split_tokens)
+    if args.kernel == 3:
+        args.two_call = True       # the fused step runs on the other kernels
+    shape = pkv.decode_shape(q, kc, bt, maxL, args.split_tokens, args.kernel)
     plan = pkv.decode_plan(shape)
     ws_buf = pkv.alloc_workspace(shape, dev)
     stream = torch.cuda.current_stream(dev)
@@ -355,7 +360,8 @@ def run_pkv(args):
         if args.two_call:
             pkv.kv_cache_append(k_in, v_in, s_in, kc, vc, stream=stream)
             pkv.paged_attn_decode(q_in, kc, vc, bt_in, cl_in, w.scale, out, max_context_len=maxL,
-                                  split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+                                  split_tokens=args.split_tokens, kernel=args.kernel,
+                                  workspace=ws_buf, stream=stream)
         else:
             pkv.decode_step(q_in, k_in, v_in, kc, vc, bt_in, cl_in, w.scale, out,
                             max_context_len=maxL, split_tokens=args.split_tokens,
@@ -385,7 +391,8 @@ def run_pkv(args):
             pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
             b.record(stream)
             pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
-                                  split_tokens=args.split_tokens, workspace=ws_buf, stream=stream)
+                                  split_tokens=args.split_tokens, kernel=args.kernel,
+                                  workspace=ws_buf, stream=stream)
         else:
             b.record(stream)
             step()
@@ -483,7 +490,7 @@ def run_pkv(args):
                    "schedule": "persistent" if plan.schedule == 1 else "partitions",
                    "grid_ctas": plan.grid_ctas,
                    "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
-                   "kernel_variant": "mma" if plan.variant else "simt",
+                   "kernel_variant": ["cuda-core", "mma.sync", "tcgen05"][plan.variant],
                    "l2": f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB L2)",
                    "parallelism": f"replicas x{ws}"},
         "pct_hbm_peak": value / ws / peak,

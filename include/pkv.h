@@ -91,9 +91,9 @@ enum {
  *                       (group 3-32), 3 tcgen05 tensor cores with TMEM
  *                       accumulators (head_dim 128, group 1-32, partition
  *                       schedule; decode only).  The library's choice: 1 for
- *                       groups of 1-2, 2 for 3-8, 3 for 9-32 at head_dim 128
- *                       (2 otherwise).  An inapplicable choice gives
- *                       PKV_ERR_UNSUPPORTED. */
+ *                       groups of 1-2, 2 for 3-32 (faster than 3 on GB300 at
+ *                       every group size measured).  An inapplicable choice
+ *                       gives PKV_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t num_seqs;
   int32_t num_q_heads;

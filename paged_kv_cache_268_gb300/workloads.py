@@ -89,6 +89,12 @@ WORKLOADS = {
     # U{1..2048} (after the append), 512-token prefixes shared by groups of 8
     "cont_batch": WorkloadSpec("cont_batch", 256, 32, 8, 128, 16, F16, 32768,
                                128, "uniform", (1, 2048), share_prefix=True),
+    # not one of the five workloads: a wide-group batch (16 query heads per kv
+    # head) for comparing the tensor-core kernels
+    "wide_gqa16": WorkloadSpec("wide_gqa16", 64, 128, 8, 128, 16, BF16, 16384, 256,
+                               "uniform", (512, 4096)),
+    "wide_gqa32": WorkloadSpec("wide_gqa32", 64, 256, 8, 128, 16, BF16, 16384, 256,
+                               "uniform", (512, 4096)),
 }
 ORDER = ["tiny_mha", "llama7b_mha", "llama3_8b_gqa", "long_ctx_gqa", "cont_batch"]
 
