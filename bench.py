@@ -66,6 +66,9 @@ def parse_args(argv=None):
     p.add_argument("--copy-bench", action="store_true",
                    help="also time pkv_copy_blocks (device->device, device->pinned host, "
                         "pinned host->device) on blocks of this workload's shape")
+    p.add_argument("--graph", action="store_true",
+                   help="capture one step in a CUDA graph and replay it (cuts host launch "
+                        "overhead for small batches)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -357,15 +360,16 @@ def run_pkv(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(k_in=k_new, v_in=v_new, s_in=slots, q_in=q, bt_in=bt, cl_in=cl):
+        st = torch.cuda.current_stream(dev)     # the capture stream inside a CUDA graph
         if args.two_call:
-            pkv.kv_cache_append(k_in, v_in, s_in, kc, vc, stream=stream)
+            pkv.kv_cache_append(k_in, v_in, s_in, kc, vc, stream=st)
             pkv.paged_attn_decode(q_in, kc, vc, bt_in, cl_in, w.scale, out, max_context_len=maxL,
                                   split_tokens=args.split_tokens, kernel=args.kernel,
-                                  workspace=ws_buf, stream=stream)
+                                  workspace=ws_buf, stream=st)
         else:
             pkv.decode_step(q_in, k_in, v_in, kc, vc, bt_in, cl_in, w.scale, out,
                             max_context_len=maxL, split_tokens=args.split_tokens,
-                            workspace=ws_buf, stream=stream)
+                            workspace=ws_buf, stream=st)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -383,11 +387,22 @@ def run_pkv(args):
     torch.cuda.synchronize()
     n0 = pkv.launch_count()
     t_host0 = time.time()
-    start.record(stream)
+    start.record(stream)     # re-recorded after capture when --graph
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        start.record(stream)
     for i in range(K):
         a, b, c = ev[i]
         a.record(stream)
-        if args.two_call:
+        if graph is not None:
+            b.record(stream)
+            graph.replay()
+        elif args.two_call:
             pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
             b.record(stream)
             pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
@@ -400,7 +415,9 @@ def run_pkv(args):
     end.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
-    launches = pkv.launch_count() - n0
+    # launches made through the library (a graph replays its captured kernels
+    # without calling the library: 2 kernels per replayed step)
+    launches = pkv.launch_count() - n0 if graph is None else (pkv.launch_count() - n0) * K
     if dist:
         dist.barrier()
     if sampler:
@@ -492,7 +509,8 @@ def run_pkv(args):
                    "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
                    "kernel_variant": ["cuda-core", "mma.sync", "tcgen05"][plan.variant],
                    "l2": f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB L2)",
-                   "parallelism": f"replicas x{ws}"},
+                   "parallelism": f"replicas x{ws}",
+                   "cuda_graph": bool(args.graph)},
         "pct_hbm_peak": value / ws / peak,
         "seq_tokens_per_s": job["seqs"] * K / (total_ms * 1e-3),
         "context_tokens_per_s": job["ctx_tokens"] * K / (total_ms * 1e-3),
