@@ -200,7 +200,8 @@ def build_workload(args, rank: int, device):
     if args.num_seqs and args.num_seqs != spec.num_seqs:
         # same length distribution, heads and pool density; fewer sequences
         n = args.num_seqs
-        largs = spec.len_args[:n] if spec.lens == "fixed" else spec.len_args
+        largs = (tuple(spec.len_args[i % len(spec.len_args)] for i in range(n))
+                 if spec.lens == "fixed" else spec.len_args)
         spec = replace(spec, name=f"{spec.name}/{n}", num_seqs=n, len_args=largs,
                        num_blocks=max(64, -(-spec.num_blocks * n // spec.num_seqs)))
     return W.make(spec, seed=args.seed + rank, device=device)

@@ -936,49 +936,72 @@ __global__ void __launch_bounds__(256)
 
 // Cross-split reduce: one warp per (sequence, query head) with more than one
 // split.  M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
-// summed in split order (deterministic).
+// summed in split order (deterministic).  Lane j holds (m, l) of split j (of
+// each group of 32 splits) and hands w_j to the others by shuffle; each lane
+// owns D / 32 output elements and keeps the loads of up to 16 partials in
+// flight, so a row costs a few L2 round trips rather than one per split.
 template <bool BF, int D>
 __global__ void __launch_bounds__(256)
     split_reduce_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                         const int32_t* __restrict__ context_lens, uint16_t* __restrict__ out,
                         int B, int Hq, int S, int P, int max_ctx) {
-  constexpr int OPL = D / 32;
-  pdl_wait();
+  constexpr int OPL = D / 32;               // output elements per lane: 2, 4 or 8
+  constexpr int J = OPL >= 8 ? 8 : 16;      // partials loaded per batch
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (gw >= B * Hq) return;
-  const int seq = gw / Hq;
-  const int L = context_lens[seq];
-  if (L < 1 || L > max_ctx) return;
-  const int n = (L + P - 1) / P;
+  // The lengths were written before the decode grid started, so they can be
+  // read before waiting for it; the partials only after.
+  int n = 0;
+  if (gw < B * Hq) {
+    const int L = context_lens[gw / Hq];
+    if (L >= 1 && L <= max_ctx) n = (L + P - 1) / P;
+  }
+  pdl_wait();
   if (n <= 1) return;
   const float2* ml = part_ml + (size_t)gw * S;
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, ml[s].x);
+  const float2 first = lane < n ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+  float M = first.x;
+  for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+
   float lsum = 0.f;
-  for (int s = lane; s < n; s += 32) lsum = fmaf(fast_exp2(ml[s].x - M), ml[s].y, lsum);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
   float acc[OPL];
 #pragma unroll
   for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
   const float* po = part_o + (size_t)gw * S * D + lane * OPL;
-  for (int s = 0; s < n; ++s) {
-    const float w = fast_exp2(ml[s].x - M);
-    if constexpr (OPL == 2) {
-      const float2 v = *reinterpret_cast<const float2*>(po + (size_t)s * D);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-    } else {
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const bool mine = s0 + lane < n;
+    const float2 v = s0 == 0 ? first : (mine ? __ldcg(ml + s0 + lane) : make_float2(0.f, 0.f));
+    const float w = mine ? fast_exp2(v.x - M) : 0.f;
+    if (mine) lsum = fmaf(w, v.y, lsum);
+    const int cnt = min(32, n - s0);
+    for (int j0 = 0; j0 < cnt; j0 += J) {
+      float x[J][OPL];
 #pragma unroll
-      for (int e = 0; e < OPL; e += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(po + (size_t)s * D + e);
-        acc[e] = fmaf(w, v.x, acc[e]); acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
-        acc[e + 2] = fmaf(w, v.z, acc[e + 2]); acc[e + 3] = fmaf(w, v.w, acc[e + 3]);
+      for (int j = 0; j < J; ++j) {
+        if (j0 + j < cnt) {
+          const float* src = po + (size_t)(s0 + j0 + j) * D;
+#pragma unroll
+          for (int e = 0; e < OPL; e += 2) {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src + e));
+            x[j][e] = t.x;
+            x[j][e + 1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const float wj = __shfl_sync(kFull, w, (j0 + j) & 31);
+        if (j0 + j < cnt) {
+#pragma unroll
+          for (int e = 0; e < OPL; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
+        }
       }
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
   uint16_t* orow = out + (size_t)gw * D + lane * OPL;
 #pragma unroll
   for (int e = 0; e < OPL; ++e) orow[e] = to_elem<BF>(acc[e] / lsum);
