@@ -313,8 +313,9 @@ int pick_variant(const pkv_shape* s, bool fused) {
     case 3: return tc_ok ? 2 : -1;
     default:
       // Measured on GB300: mma.sync stays ahead of the tcgen05 kernel at every
-      // group size (0.90 vs 0.51 of HBM peak at group 4, 0.78 vs 0.52 at 16,
-      // 0.57 vs 0.25 at 32), so the library's choice never takes tcgen05.
+      // group size (fraction of HBM peak: 0.92 vs 0.61 at group 4, 0.89 vs
+      // 0.88 at 8 on the long-context batch, 0.75 vs 0.72 at 16, 0.54 vs 0.52
+      // at 32), so the library's choice never takes tcgen05.
       return G <= 2 ? 0 : 1;
   }
 }
@@ -327,8 +328,8 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan, bool fused = false) {
   KernelGeometry geo{};
   decode_geometry(s->head_dim, bs, plan->variant, &geo);
   if (plan->variant == 2) {
-    geo.warps = 4;
-    geo.stages = 3;   // tile slots of 128 tokens
+    geo.warps = tc_warps(G);
+    geo.stages = tc_ring_slots(G);   // K/V tile slots of 128 tokens
     geo.smem_bytes = tc_smem_bytes(G);
   }
   plan->warps_per_cta = geo.warps;
@@ -363,7 +364,9 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan, bool fused = false) {
     // the whole grid would be under four waves, wave quantisation dominates
     // instead: use exactly one wave of equal partitions.
     const long long slots = static_cast<long long>(sms) * ctas_per_sm_for(geo.smem_bytes);
-    P = 1024;
+    // the tcgen05 kernel's CTAs start up slower (TMEM, a deeper ring, fewer
+    // CTAs per SM): 2048-token partitions, 4096 where one CTA fills an SM
+    P = plan->variant == 2 ? (G > 16 ? 4096 : 2048) : 1024;
     if (units > 0 && units * ((maxL + P - 1) / P) < 4 * slots) {
       const long long S = slots / units > 0 ? slots / units : 1;
       P = (maxL + S - 1) / S;

@@ -21,7 +21,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
     mask |= 1 << dev;
   }
   const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * a.S;
-  kern<<<grid, 128, SMEM, stream>>>(a, tk, tv);
+  kern<<<grid, TcLayout<N>::THREADS, SMEM, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
@@ -46,5 +46,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& tk, const C
 }
 
 int tc_smem_bytes(int G) { return G > 16 ? TcLayout<32>::BYTES : TcLayout<16>::BYTES; }
+int tc_ring_slots(int G) { return G > 16 ? TcLayout<32>::SLOTS : TcLayout<16>::SLOTS; }
+int tc_warps(int G) { return (G > 16 ? TcLayout<32>::THREADS : TcLayout<16>::THREADS) / 32; }
 
 }  // namespace pkv

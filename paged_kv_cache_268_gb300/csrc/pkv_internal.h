@@ -71,6 +71,8 @@ cudaError_t launch_decode_bf16_mma(const DecodeArgs&, const CUtensorMap&, const 
 cudaError_t launch_decode_tc(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&, bool bf16,
                              int head_dim, int block_size, cudaStream_t);
 int tc_smem_bytes(int group_size);
+int tc_ring_slots(int group_size);   // 32 KB K/V tile slots per CTA
+int tc_warps(int group_size);        // warps per CTA (softmax, producer, MMA)
 
 int* device_error_word();  // device address of the error word (current device)
 
