@@ -237,3 +237,52 @@ def test_kernel_choice_rules(pkv):
         pkv.decode_plan(shp(1))                          # CUDA cores need group <= 2
     with pytest.raises(pkv.PkvError):
         pkv.decode_plan(shp(3, -1))                      # tcgen05 has no persistent schedule
+
+
+@pytest.mark.parametrize("kernel", [0, 3])
+@pytest.mark.parametrize("G", [8, 32])
+def test_rising_logits_rescale(pkv, kernel, G):
+    """K rows scaled up along each sequence make the logits keep growing, so
+    the running maxima rise again and again: the rescale of the partial
+    output (in registers for mma.sync, in TMEM for tcgen05) runs many times
+    within one partition."""
+    Hkv, bs = 2, 16
+    spec = W.WorkloadSpec("ramp", 3, G * Hkv, Hkv, 128, bs, W.BF16, 0, 0, "uniform", (1, 1))
+    lens = np.array([700, 1300, 2100], dtype=np.int32)
+    spec = W.scaled(spec, 3, int(lens.max()))
+    w = W.make(spec, seed=17 + G, lens=lens)
+    for i, L in enumerate(lens):
+        t = np.arange(int(L))
+        f = torch.from_numpy((1.0 + t / 96.0).astype(np.float32)).to(torch.bfloat16)
+        blocks = torch.from_numpy(w.block_tables[i, t // bs].astype(np.int64))
+        offs = torch.from_numpy((t % bs).astype(np.int64))
+        rows = w.k_cache[blocks, :, offs, :]                   # [L, Hkv, D]
+        w.k_cache[blocks, :, offs, :] = (rows.float() * f.float()[:, None, None]).to(torch.bfloat16)
+    d = device_inputs(w)
+    ref = oracle_decode(w)
+    for split in (0, 1 << 20):
+        out = pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                    d["context_lens"], w.scale, max_context_len=w.max_context_len,
+                                    split_tokens=split, kernel=kernel)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert_close(widen_out(out), ref, f"rising logits kernel={kernel} G={G} split={split}")
+
+
+def test_tcgen05_bad_block_id(pkv):
+    """The tcgen05 kernel's range check: the unit is skipped, the error word is
+    set, TMEM is released (the next call on the same GPU runs normally)."""
+    w = W.make(SMALL["long_ctx_gqa"], seed=2)
+    d = device_inputs(w)
+    d["block_tables"][1, 3] = w.spec.num_blocks + 5
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], w.scale, max_context_len=w.max_context_len, kernel=3)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 1
+    d["block_tables"][1, 3] = int(w.block_tables[1, 3])
+    out = pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], w.scale, max_context_len=w.max_context_len,
+                                kernel=3)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert_close(widen_out(out), oracle_decode(w), "tcgen05 after a bad block id")
