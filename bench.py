@@ -360,15 +360,15 @@ def run_pkv(args):
     ws_buf = pkv.alloc_workspace(shape, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(k_in=k_new, v_in=v_new, s_in=slots, q_in=q, bt_in=bt, cl_in=cl):
+    def step(k_in=k_new, v_in=v_new, s_in=slots, q_in=q, bt_in=bt, cl_in=cl, out_t=out):
         st = torch.cuda.current_stream(dev)     # the capture stream inside a CUDA graph
         if args.two_call:
             pkv.kv_cache_append(k_in, v_in, s_in, kc, vc, stream=st)
-            pkv.paged_attn_decode(q_in, kc, vc, bt_in, cl_in, w.scale, out, max_context_len=maxL,
+            pkv.paged_attn_decode(q_in, kc, vc, bt_in, cl_in, w.scale, out_t, max_context_len=maxL,
                                   split_tokens=args.split_tokens, kernel=args.kernel,
                                   workspace=ws_buf, stream=st)
         else:
-            pkv.decode_step(q_in, k_in, v_in, kc, vc, bt_in, cl_in, w.scale, out,
+            pkv.decode_step(q_in, k_in, v_in, kc, vc, bt_in, cl_in, w.scale, out_t,
                             max_context_len=maxL, split_tokens=args.split_tokens,
                             workspace=ws_buf, stream=st)
 
@@ -380,53 +380,73 @@ def run_pkv(args):
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.2 if sampler else 0)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph = None
+    per_replay = 0
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        c0 = pkv.launch_count()
+        with torch.cuda.graph(graph):
+            step()
+        per_replay = pkv.launch_count() - c0     # kernels captured in one step
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def one_step(marks=None):
+        """One timed step; `marks` = (before, between append and decode, after)
+        events, recorded only in the breakdown pass."""
+        if marks:
+            marks[0].record(stream)
+        if graph is not None:
+            if marks:
+                marks[1].record(stream)
+            graph.replay()
+        elif args.two_call:
+            pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
+            if marks:
+                marks[1].record(stream)
+            pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
+                                  split_tokens=args.split_tokens, kernel=args.kernel,
+                                  workspace=ws_buf, stream=stream)
+        else:
+            if marks:
+                marks[1].record(stream)
+            step()
+        if marks:
+            marks[2].record(stream)
+
+    # The timed region: K steps back to back between two events (no events
+    # between steps, which would add their own gaps).
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     n0 = pkv.launch_count()
     t_host0 = time.time()
-    start.record(stream)     # re-recorded after capture when --graph
-    graph = None
-    if args.graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        graph.replay()
-        torch.cuda.synchronize()
-        start.record(stream)
+    start.record(stream)
     for i in range(K):
-        a, b, c = ev[i]
-        a.record(stream)
-        if graph is not None:
-            b.record(stream)
-            graph.replay()
-        elif args.two_call:
-            pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
-            b.record(stream)
-            pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
-                                  split_tokens=args.split_tokens, kernel=args.kernel,
-                                  workspace=ws_buf, stream=stream)
-        else:
-            b.record(stream)
-            step()
-        c.record(stream)
+        one_step()
     end.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
     # launches made through the library (a graph replays its captured kernels
-    # without calling the library: 2 kernels per replayed step)
-    launches = pkv.launch_count() - n0 if graph is None else (pkv.launch_count() - n0) * K
+    # without calling the library)
+    launches = pkv.launch_count() - n0 if graph is None else per_replay * K
     if dist:
         dist.barrier()
     if sampler:
         sampler.stop()
     total_ms = start.elapsed_time(end)
-    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    append_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     assert pkv.get_device_error() == 0
+
+    # Per-step breakdown (median / P90 and the append share), after the timed
+    # region: each step bracketed by events.
+    nb = min(K, 200)
+    marks = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(nb)]
+    for i in range(nb):
+        one_step(marks[i])
+    torch.cuda.synchronize()
+    decode_ms = [m[1].elapsed_time(m[2]) for m in marks]
+    append_ms = [m[0].elapsed_time(m[1]) for m in marks]
 
     kv_bytes = w.kv_bytes()
     total_ms, job = job_totals(dist, dev, total_ms,
@@ -435,50 +455,85 @@ def run_pkv(args):
     ms_per_step = total_ms / K
     value = job["kv_bytes"] * K / (total_ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    dec_avg = sum(decode_ms) / K
-    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
+    # this rank's average step (decode kernel + split reduce, append fused)
+    # over the timed region
+    achieved = kv_bytes * K / (start.elapsed_time(end) * 1e-3) / 1e9
 
-    # end-to-end through the public API with pinned host buffers: per step,
-    # copy this step's inputs host->device, run append + decode, read out back
+    # end-to-end through the public API with pinned host buffers: every step
+    # copies its inputs host->device, runs append + decode and reads its output
+    # back.  As a serving loop would, the copies run on a second stream and
+    # overlap the neighbouring steps' kernels: step i+1's inputs go up and
+    # step i's output comes down while the GPU computes (inputs and outputs
+    # are double-buffered).  The timed region spans every copy of every step.
     e2e = None
     if not args.no_e2e:
         h_q = q.cpu().pin_memory()
         h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
         h_slots = slots.cpu().pin_memory()
         h_bt, h_cl = bt.cpu().pin_memory(), cl.cpu().pin_memory()
-        h_out = torch.empty_like(h_q).pin_memory()
-        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-        d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
-        pairs = [(d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_cl, h_cl)]
-        if args.two_call:
-            pairs.append((d_slots, h_slots))      # the fused step derives the slots itself
-        h2d = sum(h.numel() * h.element_size() for _, h in pairs)
-        d2h = h_out.numel() * h_out.element_size()
-
-        def e2e_step():
-            for d, h in pairs:
-                d.copy_(h, non_blocking=True)
-            step(d_k, d_v, d_slots, d_q, d_bt, d_cl)
-            h_out.copy_(out, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
+        hosts = [h_q, h_k, h_v, h_slots, h_bt, h_cl]
+        sets = [[torch.empty_like(t, device=dev) for t in (q, k_new, v_new, slots, bt, cl)]
+                for _ in range(2)]
+        outs = [torch.empty_like(out) for _ in range(2)]
+        h_outs = [torch.empty_like(h_q).pin_memory() for _ in range(2)]
+        up = [0, 1, 2, 4, 5] + ([3] if args.two_call else [])  # the fused step derives the slots
+        h2d = sum(hosts[j].numel() * hosts[j].element_size() for j in up)
+        d2h = h_outs[0].numel() * h_outs[0].element_size()
+        xs = torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()
         Ke = max(10, min(K, 500))
+
+        def run_e2e(n):
+            in_ready, computed, drained = [ev(), None], [None, None], [None, None]
+            with torch.cuda.stream(xs):
+                xs.wait_stream(stream)
+                for j in up:
+                    sets[0][j].copy_(hosts[j], non_blocking=True)
+                in_ready[0].record(xs)
+            for i in range(n):
+                b = i & 1
+                stream.wait_event(in_ready[b])
+                if drained[b] is not None:
+                    stream.wait_event(drained[b])        # out[b] of step i-2 is on the host
+                dq, dk, dv, dsl, dbt, dcl = sets[b]
+                step(dk, dv, dsl, dq, dbt, dcl, outs[b])
+                computed[b] = ev()
+                computed[b].record(stream)
+                with torch.cuda.stream(xs):
+                    if i + 1 < n:
+                        nb = b ^ 1
+                        if i >= 1:
+                            xs.wait_event(computed[nb])  # step i-1 is done with set nb
+                        for j in up:
+                            sets[nb][j].copy_(hosts[j], non_blocking=True)
+                        in_ready[nb] = ev()
+                        in_ready[nb].record(xs)
+                    xs.wait_event(computed[b])
+                    h_outs[b].copy_(outs[b], non_blocking=True)
+                    drained[b] = ev()
+                    drained[b].record(xs)
+            stream.wait_stream(xs)
+
+        run_e2e(4)
+        torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         s0.record(stream)
-        for _ in range(Ke):
-            e2e_step()
+        run_e2e(Ke)
         s1.record(stream)
         torch.cuda.synchronize()
         e_ms, ejob = job_totals(dist, dev, s0.elapsed_time(s1), {"kv_bytes": kv_bytes})
-        assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+        ref_out = torch.empty_like(out)
+        step(out_t=ref_out)
+        torch.cuda.synchronize()
+        assert torch.equal(h_outs[(Ke - 1) & 1].view(torch.int16), ref_out.cpu().view(torch.int16))
         e2e = {"value": ejob["kv_bytes"] * Ke / (e_ms * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
-               "ms_per_step": e_ms / Ke}
+               "ms_per_step": e_ms / Ke,
+               "copies": "pinned host <-> device on a second stream, overlapping the "
+                         "neighbouring steps' kernels (double-buffered inputs and outputs)"}
 
     if rank != 0:
         if dist:
