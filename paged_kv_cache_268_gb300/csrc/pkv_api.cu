@@ -29,6 +29,9 @@ __global__ void __launch_bounds__(256)
                      const int32_t* __restrict__ slot_mapping, uint4* __restrict__ k_cache,
                      uint4* __restrict__ v_cache, int T, int Hkv, int bs, int NB,
                      int chunks_per_row, int* err) {
+  // a decode launched next on the stream may become resident meanwhile; it
+  // waits for this grid before reading the cache
+  pdl_launch_dependents();
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<long long>(T) * Hkv) return;

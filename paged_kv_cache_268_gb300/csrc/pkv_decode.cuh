@@ -470,6 +470,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
   idx /= a.S;
   const int kvh = idx % a.Hkv;
   const int seq = idx / a.Hkv;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  // The grid is launched as a programmatic dependent of the previous kernel
+  // on the stream (the last step's reduce): it may become resident while that
+  // kernel finishes, and touches no memory before it has.
+  pdl_wait();
 
   const int L = a.context_lens[seq];
   if (L < 1 || L > a.max_ctx) {
@@ -482,10 +490,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int j0 = t0 / BS;
   const int nblk = (t1 - t0 + BS - 1) / BS;
 
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-  }
   // Block-table gather for this partition (indirect addressing), range-checked.
   bool bad = false;
   for (int k = threadIdx.x; k < nblk; k += NW * 32) {
@@ -939,7 +943,8 @@ __global__ void __launch_bounds__(256)
 // summed in split order (deterministic).  Lane j holds (m, l) of split j (of
 // each group of 32 splits) and hands w_j to the others by shuffle; each lane
 // owns D / 32 output elements and keeps the loads of up to 16 partials in
-// flight, so a row costs a few L2 round trips rather than one per split.
+// flight (the first batch together with the (m, l) loads), so a row costs a
+// couple of L2 round trips rather than one per split.
 template <bool BF, int D>
 __global__ void __launch_bounds__(256)
     split_reduce_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
@@ -947,6 +952,8 @@ __global__ void __launch_bounds__(256)
                         int B, int Hq, int S, int P, int max_ctx) {
   constexpr int OPL = D / 32;               // output elements per lane: 2, 4 or 8
   constexpr int J = OPL >= 8 ? 8 : 16;      // partials loaded per batch
+  // the next step's decode grid may become resident while this one runs
+  pdl_launch_dependents();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   // The lengths were written before the decode grid started, so they can be
@@ -959,6 +966,41 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   if (n <= 1) return;
   const float2* ml = part_ml + (size_t)gw * S;
+  const float* po = part_o + (size_t)gw * S * D + lane * OPL;
+  // partials s_begin .. s_begin + cnt - 1 (cnt <= J) into x
+  auto load = [&](float (&x)[J][OPL], int s_begin, int cnt) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      if (j < cnt) {
+        const float* src = po + (size_t)(s_begin + j) * D;
+#pragma unroll
+        for (int e = 0; e < OPL; e += 2) {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src + e));
+          x[j][e] = t.x;
+          x[j][e + 1] = t.y;
+        }
+      }
+    }
+  };
+  // acc += w_s x_s for the splits j0 .. of the current group of 32, w_s held by lane s % 32
+  float acc[OPL];
+#pragma unroll
+  for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
+  auto accumulate = [&](const float (&x)[J][OPL], float w, int j0, int cnt) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float wj = __shfl_sync(kFull, w, (j0 + j) & 31);
+      if (j0 + j < cnt) {
+#pragma unroll
+        for (int e = 0; e < OPL; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
+      }
+    }
+  };
+
+  // The first batch of partials is in flight together with the (m, l) loads.
+  float x[J][OPL];
+  const int cnt0 = min(32, n);
+  load(x, 0, min(J, cnt0));
   const float2 first = lane < n ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
   float M = first.x;
   for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
@@ -966,38 +1008,22 @@ __global__ void __launch_bounds__(256)
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
 
   float lsum = 0.f;
-  float acc[OPL];
-#pragma unroll
-  for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
-  const float* po = part_o + (size_t)gw * S * D + lane * OPL;
-  for (int s0 = 0; s0 < n; s0 += 32) {
+  float w = lane < n ? fast_exp2(first.x - M) : 0.f;
+  if (lane < n) lsum = fmaf(w, first.y, lsum);
+  accumulate(x, w, 0, cnt0);
+  for (int j0 = J; j0 < cnt0; j0 += J) {
+    load(x, j0, min(J, cnt0 - j0));
+    accumulate(x, w, j0, cnt0);
+  }
+  for (int s0 = 32; s0 < n; s0 += 32) {
     const bool mine = s0 + lane < n;
-    const float2 v = s0 == 0 ? first : (mine ? __ldcg(ml + s0 + lane) : make_float2(0.f, 0.f));
-    const float w = mine ? fast_exp2(v.x - M) : 0.f;
+    const float2 v = mine ? __ldcg(ml + s0 + lane) : make_float2(0.f, 0.f);
+    w = mine ? fast_exp2(v.x - M) : 0.f;
     if (mine) lsum = fmaf(w, v.y, lsum);
     const int cnt = min(32, n - s0);
     for (int j0 = 0; j0 < cnt; j0 += J) {
-      float x[J][OPL];
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        if (j0 + j < cnt) {
-          const float* src = po + (size_t)(s0 + j0 + j) * D;
-#pragma unroll
-          for (int e = 0; e < OPL; e += 2) {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src + e));
-            x[j][e] = t.x;
-            x[j][e + 1] = t.y;
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const float wj = __shfl_sync(kFull, w, (j0 + j) & 31);
-        if (j0 + j < cnt) {
-#pragma unroll
-          for (int e = 0; e < OPL; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
-        }
-      }
+      load(x, s0 + j0, min(J, cnt - j0));
+      accumulate(x, w, j0, cnt);
     }
   }
 #pragma unroll

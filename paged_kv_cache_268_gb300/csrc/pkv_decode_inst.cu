@@ -52,9 +52,20 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   static int mask = 0;
   cudaError_t e = configure(kern, SMEM, &mask);
   if (e != cudaSuccess) return e;
-  const unsigned g = static_cast<unsigned>(a.B) * a.Hkv * a.S;
-  kern<<<g, NW * 32, SMEM, stream>>>(a, tk, tv);
-  return cudaGetLastError();
+  // programmatic launch: the grid may become resident while the previous
+  // kernel of the stream finishes (the kernel waits for it before any access)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.Hkv * a.S);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a, tk, tv);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D, int BS>

@@ -20,9 +20,20 @@ cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
     if (e != cudaSuccess) return e;
     mask |= 1 << dev;
   }
-  const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * a.S;
-  kern<<<grid, TcLayout<N>::THREADS, SMEM, stream>>>(a, tk, tv);
-  return cudaGetLastError();
+  // programmatic launch: the grid may become resident while the previous
+  // kernel of the stream finishes (the kernel waits for it before any access)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.Hkv * a.S);
+  cfg.blockDim = dim3(TcLayout<N>::THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a, tk, tv);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <bool BF>

@@ -93,6 +93,13 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   idx /= a.S;
   const int kvh = idx % a.Hkv;
   const int seq = idx / a.Hkv;
+  if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  // launched as a programmatic dependent of the previous kernel on the
+  // stream: no memory is touched before that kernel has finished
+  pdl_wait();
   const int L = a.context_lens[seq];
   if (L < 1 || L > a.max_ctx) {
     if (tid == 0 && split == 0 && kvh == 0) record_error(a.err, kDevBadContext);
@@ -106,10 +113,6 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   const int ngroups = (t1 - t0 + 127) / 128;
   const size_t row0 = (size_t)seq * a.Hq + (size_t)kvh * a.G;
 
-  if (tid == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-  }
   bool bad = false;
   for (int k = tid; k < nblk; k += LY::THREADS) {
     const int p = __ldg(a.block_tables + (size_t)seq * a.MB + j0 + k);
