@@ -353,8 +353,6 @@ def run_pkv(args):
     k_new, v_new = w.k_new, w.v_new
     out = torch.empty_like(q)
     maxL = w.max_context_len
-    if args.kernel == 3:
-        args.two_call = True       # the fused step runs on the other kernels
     shape = pkv.decode_shape(q, kc, bt, maxL, args.split_tokens, args.kernel)
     plan = pkv.decode_plan(shape)
     ws_buf = pkv.alloc_workspace(shape, dev)
@@ -370,7 +368,7 @@ def run_pkv(args):
         else:
             pkv.decode_step(q_in, k_in, v_in, kc, vc, bt_in, cl_in, w.scale, out_t,
                             max_context_len=maxL, split_tokens=args.split_tokens,
-                            workspace=ws_buf, stream=st)
+                            kernel=args.kernel, workspace=ws_buf, stream=st)
 
     for _ in range(max(args.warmup, 3)):
         step()

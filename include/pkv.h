@@ -90,7 +90,8 @@ enum {
  *                       cores (group size 1-2), 2 mma.sync tensor cores
  *                       (group 3-32), 3 tcgen05 tensor cores with TMEM
  *                       accumulators (head_dim 128, group 1-32, partition
- *                       schedule; decode only).  The library's choice: 1 for
+ *                       schedule; decode or fused step).  The library's
+ *                       choice: 1 for
  *                       groups of 1-2, 2 for 3-32 (faster than 3 on GB300 at
  *                       every group size measured).  An inapplicable choice
  *                       gives PKV_ERR_UNSUPPORTED. */

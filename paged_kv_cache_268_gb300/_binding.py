@@ -244,10 +244,11 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
 def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                 context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None, *,
-                max_context_len: int | None = None, split_tokens: int = 0,
+                max_context_len: int | None = None, split_tokens: int = 0, kernel: int = 0,
                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Append this step's token (k_new, v_new: [B, Hkv, D]) at position L-1 of
-    every sequence and run decode attention, in one launch (plus the reduce)."""
+    every sequence and run decode attention, in one launch (plus the reduce).
+    split_tokens and kernel as for paged_attn_decode."""
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
                  (v_cache, "v_cache")):
         _dense(t, n, q.dtype)
@@ -260,7 +261,7 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         out = torch.empty_like(q)
     else:
         _dense(out, "out", q.dtype)
-    shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens)
+    shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens, kernel)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
     _check("pkv_decode_step",

@@ -306,10 +306,10 @@ int check_decode_shape(const pkv_shape* s) {
 
 // Inner-loop variant (0 CUDA cores, 1 mma.sync, 2 tcgen05) for a shape, or -1
 // when the requested one cannot run it.  The tcgen05 kernel serves the
-// partition schedule of a plain decode only.
-int pick_variant(const pkv_shape* s, bool fused) {
+// partition schedule (plain decode or fused step).
+int pick_variant(const pkv_shape* s) {
   const int G = s->num_q_heads / s->num_kv_heads;
-  const bool tc_ok = s->head_dim == 128 && G <= 32 && s->split_tokens != -1 && !fused;
+  const bool tc_ok = s->head_dim == 128 && G <= 32 && s->split_tokens != -1;
   switch (s->kernel) {
     case 1: return G <= 2 ? 0 : -1;
     case 2: return 1;
@@ -323,10 +323,10 @@ int pick_variant(const pkv_shape* s, bool fused) {
   }
 }
 
-int make_plan(const pkv_shape* s, int sms, pkv_plan* plan, bool fused = false) {
+int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   const int G = s->num_q_heads / s->num_kv_heads;
   const int bs = s->block_size;
-  plan->variant = pick_variant(s, fused);
+  plan->variant = pick_variant(s);
   if (plan->variant < 0) return PKV_ERR_UNSUPPORTED;
   KernelGeometry geo{};
   decode_geometry(s->head_dim, bs, plan->variant, &geo);
@@ -495,7 +495,7 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   rc = current_device(&d);
   if (rc != PKV_OK) return rc;
   pkv_plan plan{};
-  rc = make_plan(s, d->sms, &plan, k_new != nullptr);
+  rc = make_plan(s, d->sms, &plan);
   if (rc != PKV_OK) return rc;
   if (k_new && plan.schedule != 0) return PKV_ERR_UNSUPPORTED;
   if (plan.workspace_bytes > 0) {

@@ -30,6 +30,10 @@
 //     between two buffers, so the softmax of group g + 1 does not wait for
 //     the PV of group g.
 // At the end a softmax thread holds output dimension d = t of its 16 heads.
+// Fused append (k_new set): the CTA whose partition holds position L-1
+// writes this step's K/V row to its cache slot and, once the tiles holding
+// it have landed, the MMA thread writes it into them before the MMAs read
+// them.
 // Every wait is bounded; on a timeout each role stops, loads still in flight
 // get a bounded wait, TMEM is freed and the device error word is set.
 #pragma once
@@ -61,7 +65,8 @@ struct TcLayout {
   static constexpr int OFF_RED = OFF_BAR + ((NBAR * 8 + 15) & ~15);  // [4 warps][N] floats
   static constexpr int OFF_MISC = OFF_RED + 4 * N * 4;        // TMEM address
   static constexpr int OFF_IDS = OFF_MISC + 16;
-  static constexpr int BYTES = OFF_IDS + kMaxBlocksPerCta * 4 + 1024;
+  static constexpr int OFF_NEW = OFF_IDS + kMaxBlocksPerCta * 4;  // fused append: new K, V rows
+  static constexpr int BYTES = OFF_NEW + 2 * 128 * 2 + 1024;
   static constexpr int TMEM_COLS = 3 * N <= 64 ? 64 : 128;    // S0, S1, O
 };
 
@@ -135,6 +140,19 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
                  "r"(v.w)
                  : "memory");
   }
+  // fused append: position L-1 is in this partition
+  const bool fused = a.k_new != nullptr && L - 1 >= t0 && L - 1 < t1;
+  if (fused) {
+    for (int c = tid; c < 2 * (D / 8); c += LY::THREADS) {
+      const bool isv = c >= D / 8;
+      const int gc = isv ? c - D / 8 : c;
+      const uint4 x = *reinterpret_cast<const uint4*>((isv ? a.v_new : a.k_new) +
+                                                      ((size_t)seq * a.Hkv + kvh) * D + gc * 8);
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sb + LY::OFF_NEW + c * 16),
+                   "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
+                   : "memory");
+    }
+  }
   fence_proxy_async_smem();
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), LY::TMEM_COLS);
   if (tid == 0) fence_mbar_init();
@@ -146,6 +164,18 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
     if (tid == 0) record_error(a.err, kDevBadBlock);
     if (warp == 0) tmem_dealloc(tmem, LY::TMEM_COLS);
     return;
+  }
+  if (fused && tid < 2 * (D / 8)) {
+    // the new row to its cache slot (the ids are in range past the check)
+    const int jb = (L - 1) / BS, r = (L - 1) - jb * BS;
+    const size_t dst = (((size_t)ids[jb - j0] * a.Hkv + kvh) * BS + r) * D;
+    const bool isv = tid >= D / 8;
+    const int gc = isv ? tid - D / 8 : tid;
+    uint4 x;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                 : "r"(sb + LY::OFF_NEW + tid * 16));
+    *reinterpret_cast<uint4*>((isv ? a.v_cache : a.k_cache) + dst + gc * 8) = x;
   }
   const uint32_t tO = tmem + 2 * N;   // S buffer b at tmem + b * N
   bool fail = false;
@@ -207,10 +237,29 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
         return mbar_test_wait(bar(LY::B_PFULL + j % LY::PBUF), (j / LY::PBUF) & 1) &&
                mbar_test_wait(bar(LY::B_FULL + tV % SL), (tV / SL) & 1);
       };
+      // fused append: group and tile row of position L-1
+      const int g_new = fused ? ((L - 1) - t0) / 128 : -1;
+      const int r_new = ((L - 1) - t0) & 127;
+      auto patch = [&](uint32_t tile, int isv) {
+#pragma unroll
+        for (int gc = 0; gc < D / 8; ++gc) {
+          uint4 x;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                       : "r"(sb + LY::OFF_NEW + (isv * (D / 8) + gc) * 16));
+          const uint32_t dst =
+              tile + (gc >> 3) * 16384 + r_new * 128 + (((gc & 7) ^ (r_new & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(x.x), "r"(x.y),
+                       "r"(x.z), "r"(x.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+      };
       auto issue_s = [&](int g) {
         const int tK = tile_k(g), ks = tK % SL, b = g & 1;
-        tc_fence_after();
         const uint32_t kslot = sb + ks * LY::TILE;
+        if (g == g_new) patch(kslot, 0);
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = umma_desc_sw128(kslot + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
@@ -224,8 +273,9 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
       auto issue_pv = [&](int j) {
         const int tV = tile_v(j), vs = tV % SL, pb = j % LY::PBUF;
         const uint32_t pbuf = sb + LY::OFF_P + pb * 2 * LY::P_BYTES;
-        tc_fence_after();
         const uint32_t vslot = sb + vs * LY::TILE;
+        if (j == g_new) patch(vslot, 1);
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = umma_desc_sw128(vslot + kk * 2048, 16384, 1024);

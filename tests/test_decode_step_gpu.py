@@ -15,20 +15,20 @@ from test_decode_gpu import SMALL
 pytestmark = pytest.mark.gpu
 
 
-def _two_call(pkv, w, d):
+def _two_call(pkv, w, d, kernel=0):
     kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
     pkv.kv_cache_append(w.k_new.cuda(), w.v_new.cuda(), torch.from_numpy(w.slot_mapping).cuda(),
                         kc, vc)
     out = pkv.paged_attn_decode(d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
-                                max_context_len=w.max_context_len)
+                                max_context_len=w.max_context_len, kernel=kernel)
     return out, kc, vc
 
 
-def _fused(pkv, w, d, split_tokens=0):
+def _fused(pkv, w, d, split_tokens=0, kernel=0):
     kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
     out = pkv.decode_step(d["q"], w.k_new.cuda(), w.v_new.cuda(), kc, vc, d["block_tables"],
                           d["context_lens"], w.scale, max_context_len=w.max_context_len,
-                          split_tokens=split_tokens)
+                          split_tokens=split_tokens, kernel=kernel)
     return out, kc, vc
 
 
@@ -83,3 +83,28 @@ def test_fused_step_rejects_persistent_schedule(pkv):
     with pytest.raises(pkv.PkvError) as e:
         _fused(pkv, w, d, split_tokens=-1)
     assert e.value.code == -3
+
+
+@pytest.mark.parametrize("G", [4, 8, 32])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fused_step_tcgen05(pkv, G, bs):
+    """The tcgen05 kernel's fused append: the new row reaches its cache slot
+    and the staged K and V tiles; caches and output equal append + decode on
+    the same kernel bit for bit, and the output matches the oracle.  Lengths
+    put the new token at the start, middle and end of a 128-token group and
+    of a block."""
+    lens = np.array([1, 16, 17, 127, 128, 129, 300, 1024], dtype=np.int32)
+    spec = W.WorkloadSpec("tcstep", len(lens), G * 2, 2, 128, bs, W.BF16, 0, 0, "uniform", (1, 1))
+    spec = W.scaled(spec, len(lens), int(lens.max()))
+    w = W.make(spec, seed=3 * G + bs, lens=lens)
+    d = device_inputs(w)
+    o2, k2, v2 = _two_call(pkv, w, d, kernel=3)
+    of, kf, vf = _fused(pkv, w, d, kernel=3)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert _same(kf, k2) and _same(vf, v2), "caches differ from append + decode"
+    assert _same(of, o2), "output differs from append + decode"
+    ek, ev = oracle.append(W.bits(w.k_new), W.bits(w.v_new), w.slot_mapping,
+                           W.bits(w.k_cache), W.bits(w.v_cache))
+    assert np.array_equal(W.bits(kf), ek) and np.array_equal(W.bits(vf), ev)
+    assert_close(widen_out(of), oracle_decode(w, ek, ev), f"tcgen05 fused G={G} bs={bs}")
