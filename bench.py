@@ -287,6 +287,21 @@ def copy_bench(pkv, spec, dev, stream, n_pairs=1024, reps=20):
         torch.cuda.synchronize()
         res[name + "_gbs"] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
     assert pkv.get_device_error() == 0
+    # the copy engines on one contiguous run of the same size, for scale
+    # (pinned host <-> device, cudaMemcpyAsync through torch)
+    flat_d = torch.empty(nbytes // 2, dtype=dt, device=dev)
+    flat_h = torch.empty(nbytes // 2, dtype=dt).pin_memory()
+    for name, (a, b) in (("device_to_host", (flat_h, flat_d)), ("host_to_device", (flat_d, flat_h))):
+        for _ in range(3):
+            a.copy_(b, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            a.copy_(b, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["memcpy_contiguous_" + name + "_gbs"] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
     return res
 
 
