@@ -329,7 +329,7 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   plan->variant = pick_variant(s);
   if (plan->variant < 0) return PKV_ERR_UNSUPPORTED;
   KernelGeometry geo{};
-  decode_geometry(s->head_dim, bs, plan->variant, &geo);
+  decode_geometry(s->head_dim, bs, plan->variant, G, &geo);
   if (plan->variant == 2) {
     geo.warps = tc_warps(G);
     geo.stages = tc_ring_slots(G);   // K/V tile slots of 128 tokens
@@ -397,11 +397,11 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
 
 }  // namespace
 
-bool decode_geometry(int D, int BS, int variant, KernelGeometry* g) {
-  (void)variant;
+bool decode_geometry(int D, int BS, int variant, int G, KernelGeometry* g) {
+  const int nh = compute_heads(variant, G);
   g->warps = geo_warps(D, BS);
-  g->stages = geo_stages(D, BS);
-  g->smem_bytes = geo_smem(D, BS);
+  g->stages = part_stages(D, BS, nh);
+  g->smem_bytes = part_smem(D, BS, nh);
   return true;
 }
 

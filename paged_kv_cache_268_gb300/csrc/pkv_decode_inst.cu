@@ -32,8 +32,8 @@ template <int D, int BS, class Compute>
 cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                        int schedule, int grid, cudaStream_t stream) {
   constexpr int NW = geo_warps(D, BS);
-  constexpr int NS = geo_stages(D, BS);
   if (schedule == 1) {
+    constexpr int NS = geo_stages(D, BS);
     constexpr int SMEM_MAX = geo_persist_smem(D, BS, kPersistMaxSeqs);
     static_assert(SMEM_MAX <= 113 * 1024, "two persistent CTAs must fit on one SM");
     static_assert(ctas_per_sm_for(SMEM_MAX) >= 2, "two persistent CTAs must fit on one SM");
@@ -44,10 +44,8 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
     kern<<<grid, NW * 32, geo_persist_smem(D, BS, a.B), stream>>>(a, tk, tv);
     return cudaGetLastError();
   }
-  // the warps' (m, l, o) merge reuses the stage ring; wide groups need more
-  constexpr int RING = NW * NS * stage_bytes(D, BS);
-  constexpr int MERGE = NW * Compute::NH * (D + 2) * 4;
-  constexpr int SMEM = geo_smem(D, BS) + (MERGE > RING ? ((MERGE - RING + 15) & ~15) : 0);
+  constexpr int NS = part_stages(D, BS, Compute::NH);
+  constexpr int SMEM = part_smem(D, BS, Compute::NH);
   auto kern = paged_decode_kernel<kBF, D, BS, NW, NS, Compute>;
   static int mask = 0;
   cudaError_t e = configure(kern, SMEM, &mask);

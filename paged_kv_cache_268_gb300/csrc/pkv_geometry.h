@@ -19,13 +19,33 @@ constexpr int geo_warps(int D, int BS) {
   return stage_bytes(D, BS) <= 8192 ? 4 : (stage_bytes(D, BS) <= 16384 ? 2 : 1);
 }
 
+// Stages per warp of the persistent kernel.
 constexpr int geo_stages(int /*D*/, int /*BS*/) { return 2; }
 
+// Partition kernel, per compute variant (NH = padded heads one warp
+// produces: the group for the CUDA-core variant, 8 per n-tile for mma.sync).
+// Tensor-core tiles of 16 or more heads (8 KB stages) need so many registers
+// that only two 4-warp CTAs fit an SM; a third stage per warp restores the
+// bytes in flight per SM of three 2-stage CTAs.
+constexpr int part_stages(int D, int BS, int NH) {
+  return (geo_warps(D, BS) == 4 && NH * D >= 2048) ? 3 : 2;
+}
 // Stage ring + one mbarrier per stage + the partition's block ids + 1 KB of
-// slack for aligning the ring to the 1024-byte swizzle atom.
-constexpr int geo_smem(int D, int BS) {
-  return geo_warps(D, BS) * geo_stages(D, BS) * stage_bytes(D, BS) +
-         geo_warps(D, BS) * geo_stages(D, BS) * 8 + kMaxBlocksPerCta * 4 + 1024;
+// slack for aligning the ring to the 1024-byte swizzle atom, grown when the
+// warps' (m, l, o) merge needs more room than the ring.
+constexpr int part_smem(int D, int BS, int NH) {
+  return geo_warps(D, BS) * part_stages(D, BS, NH) * stage_bytes(D, BS) +
+         geo_warps(D, BS) * part_stages(D, BS, NH) * 8 + kMaxBlocksPerCta * 4 + 1024 +
+         (geo_warps(D, BS) * NH * (D + 2) * 4 >
+                  geo_warps(D, BS) * part_stages(D, BS, NH) * stage_bytes(D, BS)
+              ? ((geo_warps(D, BS) * NH * (D + 2) * 4 -
+                  geo_warps(D, BS) * part_stages(D, BS, NH) * stage_bytes(D, BS) + 15) &
+                 ~15)
+              : 0);
+}
+// Padded heads per warp of a variant (0 CUDA cores, 1 mma.sync) for group G.
+constexpr int compute_heads(int variant, int G) {
+  return variant == 0 ? G : 8 * (G <= 8 ? 1 : (G <= 16 ? 2 : 4));
 }
 
 // Largest batch the persistent schedule takes (its per-sequence block prefix

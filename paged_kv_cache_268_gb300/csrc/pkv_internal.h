@@ -48,7 +48,8 @@ struct KernelGeometry {
 
 // Variant: 0 = CUDA-core kernel (group size 1 or 2), 1 = mma.sync tensor-core
 // kernel (group size 1..32), 2 = tcgen05 kernel (its geometry is its own).
-bool decode_geometry(int head_dim, int block_size, int variant, KernelGeometry* g);
+bool decode_geometry(int head_dim, int block_size, int variant, int group_size,
+                     KernelGeometry* g);
 
 // Launch the decode kernel.  schedule 0: fixed partitions, grid B * Hkv * S;
 // schedule 1: persistent, `grid` CTAs.  Returns cudaErrorInvalidValue for an
