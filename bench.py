@@ -1,9 +1,13 @@
 """Benchmark: one paged-KV decode step on GB300.
 
-A step is one pass of the whole hot path over one batch: kv_cache_append of
-this step's token for every sequence (slot scatter), then paged_attn_decode
+A step is one pass of the whole hot path over one batch: the append of this
+step's token for every sequence (slot scatter), then paged decode attention
 (block-table gather, TMA staging of K/V blocks, fused QK / online softmax / PV,
-split-KV partials and the cross-split reduce).  The default workload is the
+split-KV partials and the cross-split reduce).  By default the append is fused
+into the decode kernel (decode_step); --two-call runs kv_cache_append and
+paged_attn_decode as separate calls.  The timed region holds K steps back to
+back between two CUDA events; the end-to-end leg adds every step's host
+copies through the same public API.  The default workload is the
 Llama-7B-shaped MHA decode batch (64 sequences, 32 q/kv heads, head_dim 128,
 block_size 16, fp16, context lengths uniform in [512, 4096], blocks shuffled
 over a 16384-block pool), with seeded synthetic inputs.
@@ -54,8 +58,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     p.add_argument("--kernel", type=int, default=0,
-                   help="inner loop: 0 library's choice, 1 CUDA cores, 2 mma.sync, 3 tcgen05 "
-                        "(tcgen05 runs the two-call step)")
+                   help="inner loop: 0 library's choice, 1 CUDA cores, 2 mma.sync, 3 tcgen05")
     p.add_argument("--num-seqs", type=int, default=0,
                    help="shrink the batch (and pool) for profiler captures; 0 = full workload")
     p.add_argument("--seed", type=int, default=0)
