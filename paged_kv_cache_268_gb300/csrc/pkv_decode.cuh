@@ -462,9 +462,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
   int* ids = reinterpret_cast<int*>(bars + NW * NS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // The reduce kernel may start launching once every CTA of this grid has
-  // started; it waits for this grid's completion before reading partials.
-  pdl_launch_dependents();
   int idx = blockIdx.x;
   const int split = idx % a.S;
   idx /= a.S;
@@ -476,8 +473,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
   // The grid is launched as a programmatic dependent of the previous kernel
   // on the stream (the last step's reduce): it may become resident while that
-  // kernel finishes, and touches no memory before it has.
+  // kernel finishes, and touches no memory before it has.  Only then may the
+  // reduce start launching (it reads the lengths before its own wait, so
+  // everything before this grid must be complete); it waits for this grid's
+  // completion before reading partials.
   pdl_wait();
+  pdl_launch_dependents();
 
   const int L = a.context_lens[seq];
   if (L < 1 || L > a.max_ctx) {

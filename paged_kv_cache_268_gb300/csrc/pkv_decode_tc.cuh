@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   int* ids = reinterpret_cast<int*>(smem + LY::OFF_IDS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_launch_dependents();
   int idx = blockIdx.x;
   const int split = idx % a.S;
   idx /= a.S;
@@ -103,8 +102,11 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
     tma_prefetch_desc(&tmV);
   }
   // launched as a programmatic dependent of the previous kernel on the
-  // stream: no memory is touched before that kernel has finished
+  // stream: no memory is touched before that kernel has finished, and the
+  // reduce (which reads the lengths before its own wait) may launch only
+  // after that
   pdl_wait();
+  pdl_launch_dependents();
   const int L = a.context_lens[seq];
   if (L < 1 || L > a.max_ctx) {
     if (tid == 0 && split == 0 && kvh == 0) record_error(a.err, kDevBadContext);
