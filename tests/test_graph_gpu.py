@@ -14,19 +14,24 @@ from test_decode_gpu import SMALL
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("kernel", [0, 3])
 @pytest.mark.parametrize("name", ["llama7b_mha", "llama3_8b_gqa", "long_ctx_gqa"])
-def test_graph_replay_matches_eager(pkv, name):
+def test_graph_replay_matches_eager(pkv, name, kernel):
+    """kernel 0: the library's choice; 3: the tcgen05 kernel (its own
+    programmatic launch and fused append inside the graph)."""
     w = W.make(SMALL[name], seed=3)
     d = device_inputs(w)
     kn, vn = w.k_new.cuda(), w.v_new.cuda()
-    shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len)
+    shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len, 0,
+                             kernel)
     ws = pkv.alloc_workspace(shape)
 
     def step(kc, vc, out, out2):
         pkv.decode_step(d["q"], kn, vn, kc, vc, d["block_tables"], d["context_lens"], w.scale,
-                        out, max_context_len=w.max_context_len, workspace=ws)
+                        out, max_context_len=w.max_context_len, kernel=kernel, workspace=ws)
         pkv.paged_attn_decode(d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
-                              out2, max_context_len=w.max_context_len, workspace=ws)
+                              out2, max_context_len=w.max_context_len, kernel=kernel,
+                              workspace=ws)
 
     kc_e, vc_e = d["k_cache"].clone(), d["v_cache"].clone()
     o_e, o2_e = torch.empty_like(d["q"]), torch.empty_like(d["q"])
