@@ -325,6 +325,16 @@ int pkv_workspace_bytes(const pkv_shape* shape, size_t* bytes);
  * the last read). */
 int pkv_get_device_error(int32_t* code, pkv_stream_t stream);
 
+/*
+ * Self-test of the bounded waits every kernel uses.  One warp waits on an
+ * mbarrier that nothing ever arrives on, with a limit of `limit_us`
+ * microseconds (1 .. 1000000) instead of the kernels' 0.5 s, then gives up,
+ * records PKV_DEV_TIMEOUT in the device error word and exits.  The context
+ * stays usable.  It checks that a wait that runs out is reported to the host
+ * rather than hanging the GPU; it never faults or traps.
+ */
+int pkv_selftest_wait_timeout(int32_t limit_us, pkv_stream_t stream);
+
 /* Human-readable text for a PKV_ERR_* code (static storage). */
 const char* pkv_strerror(int code);
 

@@ -92,6 +92,8 @@ def load_library(path: str | None = None):
     lib.pkv_workspace_bytes.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [i32p, vp]
     lib.pkv_get_device_error.restype = ctypes.c_int
+    lib.pkv_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.pkv_selftest_wait_timeout.restype = ctypes.c_int
     lib.pkv_strerror.argtypes = [ctypes.c_int]
     lib.pkv_strerror.restype = ctypes.c_char_p
     lib.pkv_launch_count.argtypes = []
@@ -379,6 +381,14 @@ def get_device_error(stream=None) -> int:
     _check("pkv_get_device_error",
            load_library().pkv_get_device_error(ctypes.byref(code), _stream_ptr(stream)))
     return int(code.value)
+
+
+def selftest_wait_timeout(limit_us: int = 50_000, stream=None) -> None:
+    """Run the bounded-wait self-test: a warp waits on an mbarrier nothing
+    arrives on and gives up after limit_us, recording PKV_DEV_TIMEOUT (read it
+    with get_device_error)."""
+    _check("pkv_selftest_wait_timeout",
+           load_library().pkv_selftest_wait_timeout(int(limit_us), _stream_ptr(stream)))
 
 
 def launch_count() -> int:

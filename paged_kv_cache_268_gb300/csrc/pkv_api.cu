@@ -55,6 +55,20 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ------------------------------------------------------------------ self-test
+// One warp waits on an mbarrier that nothing arrives on, with the same
+// bounded wait as the decode kernels, and reports the timeout.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = mbar_wait(smem_u32(&bar), 0, limit_ns);
+  if (!__all_sync(kFull, done) && threadIdx.x == 0) record_error(err, kDevTimeout);
+}
+
 // ------------------------------------------------------------------ block copy
 // Whole-block copy between pools (copy-on-write within the GPU pool, swap-out
 // to and swap-in from a pinned CPU pool that the GPU reaches directly): pair
@@ -621,6 +635,17 @@ extern "C" int pkv_copy_blocks(const pkv_shape* s, const void* src_k, const void
       static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v),
       static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v), pairs, src_num_blocks,
       dst_num_blocks, static_cast<int>(chunks), d->err);
+  g_launches.fetch_add(1);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_selftest_wait_timeout(int32_t limit_us, pkv_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return PKV_ERR_INVALID;
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      d->err, static_cast<unsigned long long>(limit_us) * 1000ull);
   g_launches.fetch_add(1);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

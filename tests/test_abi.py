@@ -85,6 +85,11 @@ def test_append_rejects_bad_args(lib):
     assert lib.pkv_launch_count() == 0
 
 
+def test_selftest_rejects_bad_limit_before_device(lib):
+    assert lib.pkv_selftest_wait_timeout(0, None) == -2
+    assert lib.pkv_selftest_wait_timeout(1000001, None) == -2
+
+
 def test_plan_rejects_before_device(lib):
     p = B.Plan()
     assert lib.pkv_decode_plan(None, ctypes.byref(p)) == -1

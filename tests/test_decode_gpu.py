@@ -286,3 +286,20 @@ def test_tcgen05_bad_block_id(pkv):
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
     assert_close(widen_out(out), oracle_decode(w), "tcgen05 after a bad block id")
+
+
+def test_wait_timeout_is_reported_and_gpu_stays_usable(pkv):
+    """Failure detection without a GPU fault: a warp waits on an mbarrier that
+    nothing arrives on, with the kernels' bounded wait; the wait runs out, the
+    host reads PKV_DEV_TIMEOUT, and the next decode on the same context is
+    correct."""
+    import time
+    t0 = time.time()
+    pkv.selftest_wait_timeout(20_000)
+    assert pkv.get_device_error() == 4
+    assert time.time() - t0 < 5.0
+    assert pkv.get_device_error() == 0        # read clears it
+    w = W.make(SMALL["llama3_8b_gqa"], seed=4)
+    assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), "decode after a timeout")
+    with pytest.raises(pkv.PkvError):
+        pkv.selftest_wait_timeout(0)
