@@ -194,7 +194,7 @@ int pkv_paged_attn_decode(const pkv_shape* shape, const void* q,
  *   other arguments as pkv_paged_attn_decode; k_cache and v_cache are written
  * The block that receives a sequence's new token must not be referenced by
  * another sequence of the batch (copy it first when a prefix block is shared).
- * Runs the partition schedule; split_tokens == -1 gives PKV_ERR_UNSUPPORTED.
+ * Runs under every schedule (split_tokens as for pkv_paged_attn_decode).
  */
 int pkv_decode_step(const pkv_shape* shape, const void* q, const void* k_new,
                     const void* v_new, void* k_cache, void* v_cache,

@@ -511,7 +511,6 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   pkv_plan plan{};
   rc = make_plan(s, d->sms, &plan);
   if (rc != PKV_OK) return rc;
-  if (k_new && plan.schedule != 0) return PKV_ERR_UNSUPPORTED;
   if (plan.workspace_bytes > 0) {
     if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16))
       return PKV_ERR_WORKSPACE;

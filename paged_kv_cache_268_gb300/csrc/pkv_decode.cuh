@@ -853,6 +853,30 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     last_j = mt.y;
     const uint32_t kt = wbuf + st * STAGE;
+    if (a.k_new != nullptr && mt.y == (cur_L - 1) / BS) {
+      // Fused append: this step's token (position L-1) goes to its slot in
+      // the cache and into the staged tile (as in the partition kernel).
+      const int i = cur_u / Hkv, h = cur_u - i * Hkv;
+      const int pid = a.block_tables[(size_t)i * a.MB + mt.y];
+      const int rr = (cur_L - 1) - mt.y * BS;
+      const size_t src = ((size_t)i * Hkv + h) * D;
+      const size_t dst = (((size_t)pid * Hkv + h) * BS + rr) * D;
+      const bool in_pool = pid >= 0 && pid < a.NB;   // a bad id was reported at issue
+      for (int c = lane; c < 2 * (D / 8); c += 32) {
+        const bool isv = c >= D / 8;
+        const int gc = isv ? c - D / 8 : c;
+        const uint4 xv =
+            *reinterpret_cast<const uint4*>((isv ? a.v_new : a.k_new) + src + gc * 8);
+        const uint32_t sa = (isv ? kt + TILE : kt) + tile_off<BS>(rr, gc);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sa), "r"(xv.x), "r"(xv.y),
+                     "r"(xv.z), "r"(xv.w)
+                     : "memory");
+        if (in_pool)
+          *reinterpret_cast<uint4*>((isv ? a.v_cache : a.k_cache) + dst + gc * 8) = xv;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     cs.block(kt, kt + TILE, min(BS, cur_L - mt.y * BS), a.scale_log2, lane);
     __syncwarp();
     const long long p = r + NS;

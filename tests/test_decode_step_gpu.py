@@ -77,12 +77,26 @@ def test_fused_step_full_continuous_batching(pkv):
     assert _same(kf, k2) and _same(vf, v2) and _same(of, o2)
 
 
-def test_fused_step_rejects_persistent_schedule(pkv):
-    w = W.make(SMALL["llama7b_mha"], seed=0)
+@pytest.mark.parametrize("name", W.ORDER)
+def test_fused_step_persistent_schedule(pkv, name):
+    """The persistent stream-K schedule with the append fused: equal to append
+    + decode on that schedule bit for bit, caches included, and to the
+    oracle."""
+    w = W.make(SMALL[name], seed=7)
     d = device_inputs(w)
-    with pytest.raises(pkv.PkvError) as e:
-        _fused(pkv, w, d, split_tokens=-1)
-    assert e.value.code == -3
+    kc2, vc2 = d["k_cache"].clone(), d["v_cache"].clone()
+    pkv.kv_cache_append(w.k_new.cuda(), w.v_new.cuda(), torch.from_numpy(w.slot_mapping).cuda(),
+                        kc2, vc2)
+    o2 = pkv.paged_attn_decode(d["q"], kc2, vc2, d["block_tables"], d["context_lens"], w.scale,
+                               max_context_len=w.max_context_len, split_tokens=-1)
+    of, kf, vf = _fused(pkv, w, d, split_tokens=-1)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert _same(kf, kc2) and _same(vf, vc2) and _same(of, o2)
+    ek, ev = oracle.append(W.bits(w.k_new), W.bits(w.v_new), w.slot_mapping,
+                           W.bits(w.k_cache), W.bits(w.v_cache))
+    assert np.array_equal(W.bits(kf), ek) and np.array_equal(W.bits(vf), ev)
+    assert_close(widen_out(of), oracle_decode(w, ek, ev), f"persistent fused {name}")
 
 
 @pytest.mark.parametrize("G", [4, 8, 32])
