@@ -382,9 +382,19 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
     // instead: use exactly one wave of equal partitions.
     const long long slots = static_cast<long long>(sms) * ctas_per_sm_for(geo.smem_bytes);
     // the tcgen05 kernel's CTAs start up slower (TMEM, a deeper ring, fewer
-    // CTAs per SM): 2048-token partitions, 4096 where one CTA fills an SM
-    P = plan->variant == 2 ? (G > 16 ? 4096 : 2048) : 1024;
-    if (units > 0 && units * ((maxL + P - 1) / P) < 4 * slots) {
+    // CTAs per SM): 2048-token partitions, 4096 where one CTA fills an SM.
+    // The 16- and 32-head mma.sync tiles (two CTAs per SM) also run best on
+    // 2048 (measured on one GB300: 5% faster than 1024 at 32 heads, 2% at 16;
+    // 3072 and 4096 slower again).
+    const bool wide_mma = plan->variant == 1 && G > 8;
+    if (plan->variant == 2)
+      P = G > 16 ? 4096 : 2048;
+    else
+      P = wide_mma ? 2048 : 1024;
+    // one wave when the grid would be under four waves (two for the wide
+    // mma.sync tiles, which measured faster at 3.4 waves than at one)
+    const long long min_waves = wide_mma ? 2 : 4;
+    if (units > 0 && units * ((maxL + P - 1) / P) < min_waves * slots) {
       const long long S = slots / units > 0 ? slots / units : 1;
       P = (maxL + S - 1) / S;
     }

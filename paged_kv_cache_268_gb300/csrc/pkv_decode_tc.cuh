@@ -14,17 +14,19 @@
 //     SLOTS tile slots, K one group ahead of V (K0 K1 V0 K2 V1 ... V(n-1)),
 //     the order the MMA consumes them in; a slot is refilled as soon as the
 //     MMA reading it has completed.
-//   * warp SW + 1 (one lane), MMA issuer: S^T[128 tok x N] = K . Q^T into one of
-//     two TMEM buffers (both operands K-major in shared memory), then, once
-//     the softmax warps have published P of the previous group,
-//     O^T[128 d x N] += V^T . P^T (V^T read MN-major from the V tile).  So
-//     QK of group g runs on the tensor pipe while group g-1 is in softmax.
+//   * warp SW + 1 (one lane), MMA issuer: S^T[128 tok x N] = K . Q^T into one
+//     of two TMEM buffers (both operands K-major in shared memory), and,
+//     once the softmax warps have published P of a group,
+//     O^T[128 d x N] += V^T . P^T (V^T read MN-major from the V tile),
+//     issuing whichever is ready first.  So QK of group g runs on the tensor
+//     pipe while group g-1 is in softmax.
 //   * warps 0..SW-1, softmax (SW = 4 for N = 16, 8 for N = 32): a thread owns
 //     token row t of S^T (TMEM lane t, tcgen05.ld 32x32b) for 16 heads (warps
 //     w and w + 4 share a lane quarter and split the heads): logits in log2
-//     units, masked past the context end.  The running per-head maxima m are raised only when a
-//     group exceeds them by more than 2^8, detected with one barrier
-//     reduction per group; then O and the partial sums are rescaled in TMEM.
+//     units, masked past the context end.  The running per-head maxima m are
+//     raised only when a group exceeds them by more than 2^8, detected with
+//     one barrier reduction per group; then O and the partial sums are
+//     rescaled in TMEM.
 //     P = 2^(s - m) (so P < 256) goes to shared memory as a K-major operand
 //     (bfloat16 as a hi + lo pair, binary16 as is); with N = 32 it alternates
 //     between two buffers, so the softmax of group g + 1 does not wait for
