@@ -113,8 +113,10 @@ typedef struct {
  *   schedule 0 (default): one CTA per (sequence, kv head, partition of
  *     split_tokens tokens), grid_ctas = B * Hkv * S, dispatched by the
  *     hardware as SMs free up, then a cross-partition reduce kernel when
- *     S > 1.  With split_tokens == 0 the partition is 1024 tokens, or one
- *     wave of equal partitions when the grid would be under four waves.
+ *     S > 1.  With split_tokens == 0 the partition is 1024 tokens (2048
+ *     for the 16- and 32-head mma.sync tiles, 2048/4096 for the tcgen05
+ *     kernel with 16/32 padded heads), or one wave of equal partitions when
+ *     the grid would be under four waves (two for the wide mma.sync tiles).
  *   schedule 1 (split_tokens == -1, num_seqs <= 2048): persistent kernel;
  *     every warp streams a fixed equal share of all KV blocks of the batch
  *     (plus hardware-dispatched tail chunks), and a merge kernel combines the
