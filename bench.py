@@ -6,8 +6,10 @@ step's token for every sequence (slot scatter), then paged decode attention
 split-KV partials and the cross-split reduce).  By default the append is fused
 into the decode kernel (decode_step); --two-call runs kv_cache_append and
 paged_attn_decode as separate calls.  The timed region holds K steps back to
-back between two CUDA events; the end-to-end leg adds every step's host
-copies through the same public API.  The default workload is the
+back between two CUDA events (inputs larger than L2); a batch whose KV fits in
+twice the L2 size gets an L2 flush before every step and is timed step by
+step.  The end-to-end leg adds every step's host copies through the same
+public API.  The default workload is the
 Llama-7B-shaped MHA decode batch (64 sequences, 32 q/kv heads, head_dim 128,
 block_size 16, fp16, context lengths uniform in [512, 4096], blocks shuffled
 over a 16384-block pool), with seeded synthetic inputs.
@@ -431,18 +433,42 @@ def run_pkv(args):
         if marks:
             marks[2].record(stream)
 
-    # The timed region: K steps back to back between two events (no events
-    # between steps, which would add their own gaps).
+    # Inputs that fit in L2 would be timed hot: for them every timed step is
+    # preceded by a write of twice the L2 size, and only the steps are timed.
+    kv_bytes = w.kv_bytes()
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 132 * 2**20
+    flush = (torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+             if kv_bytes < 2 * l2_bytes else None)
+
+    def timed_loop(n):
+        """n steps; returns the device time in ms.  Large inputs: back to back
+        between two events (no events between steps, which would add their
+        own gaps).  Inputs under 2x L2: an L2 flush before each step, outside
+        the per-step events."""
+        if flush is None:
+            start.record(stream)
+            for _ in range(n):
+                one_step()
+            end.record(stream)
+            torch.cuda.synchronize()
+            return start.elapsed_time(end)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            one_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    # The timed region.
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     n0 = pkv.launch_count()
     t_host0 = time.time()
-    start.record(stream)
-    for i in range(K):
-        one_step()
-    end.record(stream)
-    torch.cuda.synchronize()
+    loop_ms = timed_loop(K)
     t_host1 = time.time()
     # launches made through the library (a graph replays its captured kernels
     # without calling the library)
@@ -451,20 +477,31 @@ def run_pkv(args):
         dist.barrier()
     if sampler:
         sampler.stop()
-    total_ms = start.elapsed_time(end)
+    total_ms = loop_ms
     assert pkv.get_device_error() == 0
+    hot = None
+    if flush is not None:
+        # the same steps back to back with a warm L2, for reference
+        start.record(stream)
+        for _ in range(K):
+            one_step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        hot_ms = start.elapsed_time(end) / K
+        hot = {"ms_per_step": hot_ms, "value": kv_bytes / (hot_ms * 1e-3) / 1e9, "unit": UNIT}
 
     # Per-step breakdown (median / P90 and the append share), after the timed
     # region: each step bracketed by events.
     nb = min(K, 200)
     marks = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(nb)]
     for i in range(nb):
+        if flush is not None:
+            flush.zero_()
         one_step(marks[i])
     torch.cuda.synchronize()
     decode_ms = [m[1].elapsed_time(m[2]) for m in marks]
     append_ms = [m[0].elapsed_time(m[1]) for m in marks]
 
-    kv_bytes = w.kv_bytes()
     total_ms, job = job_totals(dist, dev, total_ms,
                                {"kv_bytes": kv_bytes, "seqs": spec.num_seqs,
                                 "ctx_tokens": int(w.context_lens.sum())})
@@ -473,7 +510,7 @@ def run_pkv(args):
     peak, peak_src = measured_peak()
     # this rank's average step (decode kernel + split reduce, append fused)
     # over the timed region
-    achieved = kv_bytes * K / (start.elapsed_time(end) * 1e-3) / 1e9
+    achieved = kv_bytes * K / (loop_ms * 1e-3) / 1e9
 
     # end-to-end through the public API with pinned host buffers: every step
     # copies its inputs host->device, runs append + decode and reads its output
@@ -550,6 +587,8 @@ def run_pkv(args):
                "ms_per_step": e_ms / Ke,
                "copies": "pinned host <-> device on a second stream, overlapping the "
                          "neighbouring steps' kernels (double-buffered inputs and outputs)"}
+        if flush is not None:
+            e2e["l2"] = "not flushed: the steps run back to back and the KV fits in L2"
 
     if rank != 0:
         if dist:
@@ -580,7 +619,10 @@ def run_pkv(args):
                    "grid_ctas": plan.grid_ctas,
                    "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
                    "kernel_variant": ["cuda-core", "mma.sync", "tcgen05"][plan.variant],
-                   "l2": f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB L2)",
+                   "l2": (f"no flush: inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step "
+                          f"vs {l2_bytes / 1e6:.0f} MB L2)" if flush is None else
+                          f"flushed: {2 * l2_bytes / 1e6:.0f} MB written before every timed step "
+                          f"(KV per step {kv_bytes / 1e6:.2f} MB fits in L2); steps timed one by one"),
                    "parallelism": f"replicas x{ws}",
                    "cuda_graph": bool(args.graph)},
         "pct_hbm_peak": value / ws / peak,
@@ -589,6 +631,7 @@ def run_pkv(args):
         "decode_ms_median": statistics.median(decode_ms),
         "decode_ms_p90": float(np.percentile(decode_ms, 90)),
         "append_us_median": 1e3 * statistics.median(append_ms) if args.two_call else None,
+        "hot_cache": hot,
         "roofline": {"bound": "hbm",
                      "kernel": ("paged_attn_decode" if args.two_call else "decode_step")
                                + " (decode kernel + split reduce)",

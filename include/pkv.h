@@ -170,8 +170,11 @@ int pkv_kv_cache_append(const pkv_shape* shape, const void* k, const void* v,
  *                     is 0), 16-byte aligned; its contents need no
  *                     initialisation.  Calls that share a workspace must not
  *                     overlap on the GPU.
- * A sequence whose length or block ids are out of range is skipped (its out
- * rows are left unwritten) and the device error word is set.  B == 0 is a
+ * A sequence whose length is out of range is skipped (its out rows are left
+ * unwritten); the partitions of a sequence that hold an out-of-range block id
+ * skip their work (the bad blocks are never read), so that sequence's out
+ * rows are undefined (left unwritten when it has a single partition).  Either
+ * way the device error word is set.  B == 0 is a
  * no-op.
  */
 int pkv_paged_attn_decode(const pkv_shape* shape, const void* q,

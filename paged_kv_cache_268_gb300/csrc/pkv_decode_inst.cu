@@ -1,5 +1,7 @@
 // Instantiates the decode kernels for one element type and one compute
 // variant; compiled once per (PKV_INST_BF16, PKV_INST_MMA) pair.
+#include <atomic>
+
 #include "pkv_decode.cuh"
 
 #ifndef PKV_INST_BF16
@@ -14,16 +16,19 @@ namespace {
 
 constexpr bool kBF = PKV_INST_BF16 != 0;
 
-// Raise a kernel's dynamic shared-memory limit once per device.
+// Raise a kernel's dynamic shared-memory limit once per device (every time
+// on devices past the 32 the mask tracks).  Threads that race here both set
+// the same attribute, which is harmless.
 template <class K>
-cudaError_t configure(K kern, int smem, int* mask) {
+cudaError_t configure(K kern, int smem, std::atomic<unsigned>* mask) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 32 && !(*mask & (1 << dev))) {
+  const unsigned bit = dev < 32 ? 1u << dev : 0u;
+  if (bit == 0 || !(mask->load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    *mask |= 1 << dev;
+    mask->fetch_or(bit, std::memory_order_release);
   }
   return cudaSuccess;
 }
@@ -38,7 +43,7 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
     static_assert(SMEM_MAX <= 113 * 1024, "two persistent CTAs must fit on one SM");
     static_assert(ctas_per_sm_for(SMEM_MAX) >= 2, "two persistent CTAs must fit on one SM");
     auto kern = paged_decode_persistent<kBF, D, BS, NW, NS, Compute>;
-    static int mask = 0;
+    static std::atomic<unsigned> mask{0};
     cudaError_t e = configure(kern, SMEM_MAX, &mask);
     if (e != cudaSuccess) return e;
     kern<<<grid, NW * 32, geo_persist_smem(D, BS, a.B), stream>>>(a, tk, tv);
@@ -47,7 +52,7 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   constexpr int NS = part_stages(D, BS, Compute::NH);
   constexpr int SMEM = part_smem(D, BS, Compute::NH);
   auto kern = paged_decode_kernel<kBF, D, BS, NW, NS, Compute>;
-  static int mask = 0;
+  static std::atomic<unsigned> mask{0};
   cudaError_t e = configure(kern, SMEM, &mask);
   if (e != cudaSuccess) return e;
   // programmatic launch: the grid may become resident while the previous

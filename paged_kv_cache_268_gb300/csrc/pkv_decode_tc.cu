@@ -1,5 +1,7 @@
 // Instantiates the tcgen05 decode kernel (head_dim 128; block size 16 or 32;
 // N = 16 or 32 padded query heads; binary16 or bfloat16).
+#include <atomic>
+
 #include "pkv_decode_tc.cuh"
 
 namespace pkv {
@@ -11,14 +13,16 @@ cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
   constexpr int SMEM = TcLayout<N>::BYTES;
   static_assert(SMEM <= 227 * 1024, "tcgen05 kernel shared memory");
   auto kern = paged_decode_tc<BF, BS, N>;
-  static int mask = 0;
+  // the shared-memory limit is raised once per device (every time past 32)
+  static std::atomic<unsigned> mask{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 32 && !(mask & (1 << dev))) {
+  const unsigned bit = dev < 32 ? 1u << dev : 0u;
+  if (bit == 0 || !(mask.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    mask |= 1 << dev;
+    mask.fetch_or(bit, std::memory_order_release);
   }
   // programmatic launch: the grid may become resident while the previous
   // kernel of the stream finishes (the kernel waits for it before any access)
