@@ -502,9 +502,13 @@ def run_pkv(args):
     decode_ms = [m[1].elapsed_time(m[2]) for m in marks]
     append_ms = [m[0].elapsed_time(m[1]) for m in marks]
 
+    # K+V bytes of the distinct cache rows a step touches (a shared prefix
+    # block counted once): what HBM has to deliver when L2 serves the repeats
+    unique_bytes = w.unique_kv_bytes()
     total_ms, job = job_totals(dist, dev, total_ms,
                                {"kv_bytes": kv_bytes, "seqs": spec.num_seqs,
-                                "ctx_tokens": int(w.context_lens.sum())})
+                                "ctx_tokens": int(w.context_lens.sum()),
+                                "unique_kv_bytes": unique_bytes})
     ms_per_step = total_ms / K
     value = job["kv_bytes"] * K / (total_ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
@@ -628,6 +632,8 @@ def run_pkv(args):
         "pct_hbm_peak": value / ws / peak,
         "seq_tokens_per_s": job["seqs"] * K / (total_ms * 1e-3),
         "context_tokens_per_s": job["ctx_tokens"] * K / (total_ms * 1e-3),
+        "unique_kv_bytes_per_step": unique_bytes,
+        "unique_kv_gbs": job["unique_kv_bytes"] * K / (total_ms * 1e-3) / 1e9,
         "decode_ms_median": statistics.median(decode_ms),
         "decode_ms_p90": float(np.percentile(decode_ms, 90)),
         "append_us_median": 1e3 * statistics.median(append_ms) if args.two_call else None,
