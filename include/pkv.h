@@ -322,6 +322,12 @@ int pkv_bm_block_tables(pkv_block_manager* m, const int64_t* seq_ids, int32_t n,
  * reads device attributes once. */
 int pkv_decode_plan(const pkv_shape* shape, pkv_plan* plan);
 
+/* pkv_decode_plan for a GB300-class device with `num_sms` SMs (> 0, else
+ * PKV_ERR_INVALID), without touching any device: plans ahead of a device and
+ * lets the split rule be checked on a host without a GPU.  pkv_decode_plan
+ * equals this call with the current device's SM count. */
+int pkv_decode_plan_for(const pkv_shape* shape, int32_t num_sms, pkv_plan* plan);
+
 /* Workspace bytes pkv_paged_attn_decode needs for `shape` (0 if none). */
 int pkv_workspace_bytes(const pkv_shape* shape, size_t* bytes);
 

@@ -88,6 +88,8 @@ def load_library(path: str | None = None):
         getattr(lib, "pkv_bm_" + n).restype = ctypes.c_int
     lib.pkv_decode_plan.argtypes = [sp, ctypes.POINTER(Plan)]
     lib.pkv_decode_plan.restype = ctypes.c_int
+    lib.pkv_decode_plan_for.argtypes = [sp, i32, ctypes.POINTER(Plan)]
+    lib.pkv_decode_plan_for.restype = ctypes.c_int
     lib.pkv_workspace_bytes.argtypes = [sp, ctypes.POINTER(sz)]
     lib.pkv_workspace_bytes.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [i32p, vp]
@@ -186,9 +188,16 @@ def decode_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Ten
                       dtype=_DT[q.dtype], split_tokens=int(split_tokens), kernel=int(kernel))
 
 
-def decode_plan(shape: Shape) -> Plan:
+def decode_plan(shape: Shape, num_sms: int | None = None) -> Plan:
+    """How a decode call will run on the current device, or, with `num_sms`,
+    on a device with that many SMs (host only, no GPU needed)."""
     plan = Plan()
-    _check("pkv_decode_plan", load_library().pkv_decode_plan(ctypes.byref(shape), ctypes.byref(plan)))
+    lib = load_library()
+    if num_sms is None:
+        _check("pkv_decode_plan", lib.pkv_decode_plan(ctypes.byref(shape), ctypes.byref(plan)))
+    else:
+        _check("pkv_decode_plan_for",
+               lib.pkv_decode_plan_for(ctypes.byref(shape), int(num_sms), ctypes.byref(plan)))
     return plan
 
 

@@ -467,6 +467,14 @@ extern "C" int pkv_decode_plan(const pkv_shape* s, pkv_plan* plan) {
   return make_plan(s, d->sms, plan);
 }
 
+extern "C" int pkv_decode_plan_for(const pkv_shape* s, int32_t num_sms, pkv_plan* plan) {
+  if (!s || !plan) return PKV_ERR_NULL;
+  if (num_sms < 1) return PKV_ERR_INVALID;
+  const int rc = check_decode_shape(s);
+  if (rc != PKV_OK) return rc;
+  return make_plan(s, num_sms, plan);
+}
+
 extern "C" int pkv_workspace_bytes(const pkv_shape* s, size_t* bytes) {
   if (!bytes) return PKV_ERR_NULL;
   pkv_plan plan{};
