@@ -231,25 +231,41 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _dense(t, n, q.dtype)
     _dense(block_tables, "block_tables", torch.int32)
     _dense(context_lens, "context_lens", torch.int32)
-    if v_cache.shape != k_cache.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
-        raise ValueError("q must be [B, Hq, D]; caches [NB, Hkv, bs, D]")
-    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
-        raise ValueError("block_tables must be [B, MB]; context_lens [B]")
+    _check_decode_extents(q, k_cache, v_cache, block_tables, context_lens)
     if out is None:
         out = torch.empty_like(q)
     else:
         _dense(out, "out", q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape [B, Hq, D]")
     shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens, kernel)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
+    else:
+        _dense(workspace, "workspace")
     lib = load_library()
     _check("pkv_paged_attn_decode",
            lib.pkv_paged_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(block_tables), _ptr(context_lens), float(scale),
-                                     _ptr(out), _ptr(workspace),
-                                     0 if workspace is None else workspace.numel(),
+                                     _ptr(out), _ptr(workspace), _nbytes(workspace),
                                      _stream_ptr(stream)))
     return out
+
+
+def _check_decode_extents(q, k_cache, v_cache, block_tables, context_lens):
+    """The library sees only pointers and the shape it is given, so the
+    tensors' extents must agree with that shape before any launch."""
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [NB, Hkv, bs, D] tensors of one shape")
+    if q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
+        raise ValueError("q must be [B, Hq, D] with the caches' head_dim")
+    if (block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0]
+            or context_lens.shape != (q.shape[0],)):
+        raise ValueError("block_tables must be [B, MB]; context_lens [B]")
+
+
+def _nbytes(t: torch.Tensor | None) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
 
 
 def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -265,6 +281,7 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         _dense(t, n, q.dtype)
     _dense(block_tables, "block_tables", torch.int32)
     _dense(context_lens, "context_lens", torch.int32)
+    _check_decode_extents(q, k_cache, v_cache, block_tables, context_lens)
     NB, Hkv, bs, D = _cache_shape(k_cache)
     if k_new.shape != (q.shape[0], Hkv, D) or v_new.shape != k_new.shape:
         raise ValueError("k_new, v_new must be [B, Hkv, D]")
@@ -272,15 +289,18 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         out = torch.empty_like(q)
     else:
         _dense(out, "out", q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape [B, Hq, D]")
     shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens, kernel)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
+    else:
+        _dense(workspace, "workspace")
     _check("pkv_decode_step",
            load_library().pkv_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k_new), _ptr(v_new),
                                           _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                           _ptr(context_lens), float(scale), _ptr(out),
-                                          _ptr(workspace),
-                                          0 if workspace is None else workspace.numel(),
+                                          _ptr(workspace), _nbytes(workspace),
                                           _stream_ptr(stream)))
     return out
 

@@ -97,3 +97,53 @@ def test_plan_rejects_before_device(lib):
     n = ctypes.c_size_t(0)
     assert lib.pkv_workspace_bytes(ctypes.byref(_shape()), None) == -1
     assert lib.pkv_workspace_bytes(ctypes.byref(_shape(num_kv_heads=3)), ctypes.byref(n)) == -2
+
+
+# ---------------------------------------------------------------- binding extents
+# The library sees only pointers and the shape built from the tensors, so the
+# binding must reject tensors whose extents disagree before anything launches.
+# On the CPU the CUDA-tensor check is lifted to reach the extent checks; a call
+# with consistent extents then reaches the library, which finds no device.
+def _decode_args(B=2, Hq=8, Hkv=2, D=64, bs=16, NB=8, MB=4):
+    import torch
+    f16 = torch.float16
+    return dict(q=torch.zeros(B, Hq, D, dtype=f16), k_cache=torch.zeros(NB, Hkv, bs, D, dtype=f16),
+                v_cache=torch.zeros(NB, Hkv, bs, D, dtype=f16),
+                block_tables=torch.zeros(B, MB, dtype=torch.int32),
+                context_lens=torch.ones(B, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("bad", ["q_head_dim", "v_cache", "tables_rows", "lens_len", "out_shape",
+                                 "k_new"])
+def test_binding_rejects_mismatched_extents(lib, monkeypatch, bad):
+    import torch
+    monkeypatch.setattr(B, "_dense", lambda *a, **k: None)
+    a = _decode_args()
+    out = None
+    if bad == "q_head_dim":
+        a["q"] = torch.zeros(2, 8, 128, dtype=torch.float16)
+    elif bad == "v_cache":
+        a["v_cache"] = torch.zeros(8, 2, 32, 64, dtype=torch.float16)
+    elif bad == "tables_rows":
+        a["block_tables"] = torch.zeros(3, 4, dtype=torch.int32)
+    elif bad == "lens_len":
+        a["context_lens"] = torch.ones(1, dtype=torch.int32)
+    elif bad == "out_shape":
+        out = torch.zeros(2, 8, 32, dtype=torch.float16)
+    k_new = torch.zeros(2, 2, 64 if bad != "k_new" else 32, dtype=torch.float16)
+    if bad != "k_new":
+        with pytest.raises(ValueError):
+            B.paged_attn_decode(a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
+                                a["context_lens"], 0.125, out, max_context_len=16)
+    with pytest.raises(ValueError):
+        B.decode_step(a["q"], k_new, k_new.clone(), a["k_cache"], a["v_cache"], a["block_tables"],
+                      a["context_lens"], 0.125, out, max_context_len=16)
+
+
+def test_binding_passes_consistent_extents_to_the_library(lib, monkeypatch):
+    monkeypatch.setattr(B, "_dense", lambda *a, **k: None)
+    a = _decode_args()
+    with pytest.raises(B.PkvError) as e:      # no GPU here: the library reports it
+        B.paged_attn_decode(a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
+                            a["context_lens"], 0.125, max_context_len=16)
+    assert e.value.code == -6
