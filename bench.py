@@ -48,6 +48,9 @@ METRIC = "paged decode-attention KV-read GB/s and % of GB300 HBM peak; seq-token
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "llama7b_mha"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e, nominal
+# the other workloads measured in the same run (``workloads`` in the JSON line)
+OTHER_WORKLOADS = ("tiny_mha", "llama3_8b_gqa", "long_ctx_gqa", "cont_batch")
 DTYPE_NAME = {W.F16: "f16", W.BF16: "bf16"}
 
 
@@ -78,6 +81,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the per-workload measurements of the other four workloads")
+    p.add_argument("--workload-seconds", type=float, default=0.25,
+                   help="least device time of each other workload's timed region")
     return p.parse_args(argv)
 
 
@@ -96,6 +103,31 @@ def measured_peak():
         return float(j["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cpu() -> dict:
+    """The host the CPU baseline runs on: logical CPUs and the CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or None,
+            "machine": platform.machine()}
 
 
 def kernel_source_hash() -> str:
@@ -310,6 +342,141 @@ def copy_bench(pkv, spec, dev, stream, n_pairs=1024, reps=20):
     return res
 
 
+def measure_workload(pkv, name: str, args, dev, stream, peak: float, l2_bytes: int,
+                     sampler=None) -> dict:
+    """One of the other workloads, measured the way the headline one is: the
+    fused step (this step's token appended for every sequence inside the
+    paged decode launch, then the split reduce), W warm-up steps, then at
+    least K steps and at least --workload-seconds of device time back to back
+    between two CUDA events (a batch whose KV fits in twice the L2 size gets
+    an L2 flush before every step and is timed step by step).  The
+    continuous-batching workload is also timed as two calls
+    (kv_cache_append, then paged_attn_decode), with the append alone timed
+    by events around it."""
+    import math
+    w = W.make(W.WORKLOADS[name], seed=args.seed, device=dev)
+    spec = w.spec
+    q, kc, vc = w.q, w.k_cache, w.v_cache
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    k_new, v_new = w.k_new, w.v_new
+    out = torch.empty_like(q)
+    maxL = w.max_context_len
+    shape = pkv.decode_shape(q, kc, bt, maxL, 0, 0)
+    plan = pkv.decode_plan(shape)
+    ws = pkv.alloc_workspace(shape, dev)
+
+    def fused():
+        pkv.decode_step(q, k_new, v_new, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
+                        workspace=ws, stream=stream)
+
+    def append():
+        pkv.kv_cache_append(k_new, v_new, slots, kc, vc, stream=stream)
+
+    def decode():
+        pkv.paged_attn_decode(q, kc, vc, bt, cl, w.scale, out, max_context_len=maxL,
+                              workspace=ws, stream=stream)
+
+    def two_call():
+        append()
+        decode()
+
+    kv_bytes = w.kv_bytes()
+    flush = (torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+             if kv_bytes < 2 * l2_bytes else None)
+
+    def region(fn, n):
+        """Device ms of n steps of fn (see the docstring for the L2 rule)."""
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    for _ in range(max(args.warmup, 3)):
+        fused()
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    est = max(region(fused, 5) / 5, 1e-3)
+    n = int(min(20000, max(args.steps, math.ceil(args.workload_seconds * 1e3 / est))))
+    if flush is not None:
+        n = min(n, 2000)
+    n0 = pkv.launch_count()
+    t0 = time.time()
+    ms = region(fused, n)
+    t1 = time.time()
+    launches = pkv.launch_count() - n0
+    step_s = ms / n * 1e-3
+    gbs = kv_bytes / step_s / 1e9
+    entry = {
+        "ms_per_step": ms / n, "steps": n, "kv_gbs": gbs, "frac": gbs / peak,
+        "frac_of_nominal_hbm": gbs / NOMINAL_HBM_GBS,
+        "seq_tokens_per_s": spec.num_seqs / step_s,
+        "context_tokens_per_s": float(w.context_lens.sum()) / step_s,
+        "kv_bytes_per_step": kv_bytes, "sum_context_len": int(w.context_lens.sum()),
+        "config": {"num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
+                   "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                   "block_size": spec.block_size, "element_type": DTYPE_NAME[spec.dtype],
+                   "pool_blocks": spec.num_blocks,
+                   "context_lens": f"{spec.lens}{tuple(spec.len_args)[:4]}"},
+        "plan": {"grid_ctas": plan.grid_ctas, "split_tokens": plan.split_tokens,
+                 "num_splits": plan.num_splits,
+                 "kernel_variant": ["cuda-core", "mma.sync", "tcgen05"][plan.variant]},
+        "step": "decode_step: append of 1 token/seq fused into paged decode",
+        "gpu_launches": launches,
+        "l2": ("no flush: inputs larger than L2" if flush is None else
+               f"flushed: {2 * l2_bytes / 1e6:.0f} MB written before every timed step; "
+               "steps timed one by one"),
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+    }
+    if spec.share_prefix:
+        unique = w.unique_kv_bytes()
+        entry["unique_kv_bytes_per_step"] = unique
+        entry["unique_kv_gbs"] = unique / step_s / 1e9
+        entry["unique_frac"] = unique / step_s / 1e9 / peak
+        for _ in range(max(args.warmup, 3)):
+            two_call()
+        torch.cuda.synchronize()
+        ms2 = region(two_call, n)
+        # the append alone: events around each call, median over <= 200 steps
+        nb = min(n, 200)
+        marks = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(nb)]
+        for m in marks:
+            if flush is not None:
+                flush.zero_()
+            m[0].record(stream)
+            append()
+            m[1].record(stream)
+            decode()
+            m[2].record(stream)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        entry["two_call"] = {
+            "ms_per_step": ms2 / n,
+            "kv_gbs": kv_bytes / (ms2 / n * 1e-3) / 1e9,
+            "unique_kv_gbs": unique / (ms2 / n * 1e-3) / 1e9,
+            "append_us_median": 1e3 * statistics.median(m[0].elapsed_time(m[1]) for m in marks),
+            "decode_us_median": 1e3 * statistics.median(m[1].elapsed_time(m[2]) for m in marks),
+            "step": "kv_cache_append(1 token/seq) then paged_attn_decode, back to back",
+        }
+    del w, q, kc, vc, ws, flush
+    torch.cuda.empty_cache()
+    return entry
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     ws, rank, local = dist_env()
@@ -475,8 +642,6 @@ def run_pkv(args):
     launches = pkv.launch_count() - n0 if graph is None else per_replay * K
     if dist:
         dist.barrier()
-    if sampler:
-        sampler.stop()
     total_ms = loop_ms
     assert pkv.get_device_error() == 0
     hot = None
@@ -603,8 +768,16 @@ def run_pkv(args):
     cpu = None
     if not args.no_cpu_baseline:
         gbs, desc, _ = OracleSampler(w).run(args.cpu_seconds)
-        cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+               **host_cpu()}
 
+    # The other four workloads, each measured on its own in this process.
+    others = None
+    if not args.no_workloads and not args.num_seqs:
+        others = {name: measure_workload(pkv, name, args, dev, stream, peak, l2_bytes, sampler)
+                  for name in OTHER_WORKLOADS if name != args.workload}
+    if sampler:
+        sampler.stop()
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
     traffic = recorded_traffic(spec.name)
     line = {
@@ -630,6 +803,8 @@ def run_pkv(args):
                    "parallelism": f"replicas x{ws}",
                    "cuda_graph": bool(args.graph)},
         "pct_hbm_peak": value / ws / peak,
+        "frac_of_nominal_hbm": value / ws / NOMINAL_HBM_GBS,
+        "nominal_hbm_gbs": NOMINAL_HBM_GBS,
         "seq_tokens_per_s": job["seqs"] * K / (total_ms * 1e-3),
         "context_tokens_per_s": job["ctx_tokens"] * K / (total_ms * 1e-3),
         "unique_kv_bytes_per_step": unique_bytes,
@@ -649,6 +824,7 @@ def run_pkv(args):
         "gpu_launches": launches,
         "block_copy": copy_res,
         "clocks": clocks,
+        "workloads": others,
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -81,20 +81,19 @@ enum {
  *   max_context_len     host-known upper bound on every context_lens[i]
  *                       (1 <= it <= MB * bs); sizes the split-KV grid
  *   dtype               pkv_dtype
- *   split_tokens        schedule choice: 0 lets the library choose the
- *                       partition size; > 0 sets the tokens per split-KV
- *                       partition (rounded up to a multiple of bs, and of 128
- *                       for the tcgen05 kernel); -1 selects the persistent
- *                       schedule (num_seqs <= 2048)
+ *   split_tokens        split-KV partition size: 0 lets the library choose;
+ *                       > 0 sets the tokens per partition (rounded up to a
+ *                       multiple of bs; the tcgen05 kernel walks a partition
+ *                       in 128-token groups, the last of which may be
+ *                       ragged).  Negative values give PKV_ERR_INVALID.
  *   kernel              inner-loop choice: 0 lets the library choose, 1 CUDA
  *                       cores (group size 1-2), 2 mma.sync tensor cores
  *                       (group 3-32), 3 tcgen05 tensor cores with TMEM
- *                       accumulators (head_dim 128, group 1-32, partition
- *                       schedule; decode or fused step).  The library's
- *                       choice: 1 for
- *                       groups of 1-2, 2 for 3-32 (faster than 3 on GB300 at
- *                       every group size measured).  An inapplicable choice
- *                       gives PKV_ERR_UNSUPPORTED. */
+ *                       accumulators (head_dim 128, group 1-32; decode or
+ *                       fused step).  The library's choice: 1 for groups
+ *                       of 1-2, 2 for 3-32 (faster than 3 on GB300 at every
+ *                       group size measured).  An inapplicable choice gives
+ *                       PKV_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -109,22 +108,18 @@ typedef struct {
   int32_t kernel;
 } pkv_shape;
 
-/* How a decode call will run (filled by pkv_decode_plan).
- *   schedule 0 (default): one CTA per (sequence, kv head, partition of
- *     split_tokens tokens), grid_ctas = B * Hkv * S, dispatched by the
- *     hardware as SMs free up, then a cross-partition reduce kernel when
- *     S > 1.  With split_tokens == 0 the partition is 1024 tokens (2048
- *     for the 16- and 32-head mma.sync tiles, 2048/4096 for the tcgen05
- *     kernel with 16/32 padded heads), or one wave of equal partitions when
- *     the grid would be under four waves (two for the wide mma.sync tiles).
- *   schedule 1 (split_tokens == -1, num_seqs <= 2048): persistent kernel;
- *     every warp streams a fixed equal share of all KV blocks of the batch
- *     (plus hardware-dispatched tail chunks), and a merge kernel combines the
- *     units a share boundary cut. */
+/* How a decode call will run (filled by pkv_decode_plan).  One CTA per
+ * (sequence, kv head, partition of split_tokens tokens), grid_ctas =
+ * B * Hkv * S, dispatched by the hardware as SMs free up, then a
+ * cross-partition reduce kernel when S > 1.  With split_tokens == 0 the
+ * partition is 1024 tokens (2048 for the 16- and 32-head mma.sync tiles,
+ * 2048/4096 for the tcgen05 kernel with 16/32 padded heads), or one wave of
+ * equal partitions when the grid would be under four waves (two for the wide
+ * mma.sync tiles). */
 typedef struct {
-  int32_t schedule;
-  int32_t split_tokens;     /* P, tokens per partition (schedule 0; else 0) */
-  int32_t num_splits;       /* S = ceil(max_context_len / P) (schedule 0; else 0) */
+  int32_t schedule;         /* always 0 (the partition schedule) */
+  int32_t split_tokens;     /* P, tokens per partition */
+  int32_t num_splits;       /* S = ceil(max_context_len / P) */
   int32_t variant;          /* 0 = CUDA-core kernel, 1 = mma.sync tensor-core
                                kernel, 2 = tcgen05 tensor-core kernel */
   int32_t warps_per_cta;
@@ -132,6 +127,19 @@ typedef struct {
   int32_t grid_ctas;
   size_t workspace_bytes;   /* 0 when no partials are needed */
 } pkv_plan;
+
+/*
+ * Set the split-KV workspace that decode calls on the current device use
+ * when they are given a NULL workspace (the library never allocates device
+ * memory itself).  dev_ptr: caller-owned memory of the current device,
+ * 16-byte aligned, `bytes` long (size it with pkv_workspace_bytes for the
+ * largest shape in use); the library keeps the pointer, not the memory, so
+ * keep it alive until it is replaced or cleared.  NULL clears the setting.
+ * PKV_ERR_INVALID for bytes == 0 or a pointer that is not memory of the
+ * current device, PKV_ERR_ALIGN for a misaligned one.  Calls that use the
+ * set workspace must not overlap on the GPU.
+ */
+int pkv_set_workspace(void* dev_ptr, size_t bytes);
 
 /*
  * KV append (slot scatter).  For every token t in [0, num_tokens) with
@@ -166,10 +174,14 @@ int pkv_kv_cache_append(const pkv_shape* shape, const void* k, const void* v,
  *                     appended in this step
  *   scale             softmax scale (typically 1 / sqrt(D))
  *   workspace         caller-owned device scratch for split-KV partials, at
- *                     least pkv_plan.workspace_bytes (may be NULL when that
- *                     is 0), 16-byte aligned; its contents need no
- *                     initialisation.  Calls that share a workspace must not
- *                     overlap on the GPU.
+ *                     least pkv_plan.workspace_bytes, 16-byte aligned; its
+ *                     contents need no initialisation.  NULL takes the
+ *                     workspace set for the current device with
+ *                     pkv_set_workspace (and workspace_bytes is ignored).
+ *                     Calls that share a workspace must not overlap on the
+ *                     GPU.  PKV_ERR_WORKSPACE, enqueuing nothing, when the
+ *                     call needs partials (workspace_bytes > 0 in its plan)
+ *                     and the workspace is missing, misaligned or too small.
  * A sequence whose length is out of range is skipped (its out rows are left
  * unwritten); the partitions of a sequence that hold an out-of-range block id
  * skip their work (the bad blocks are never read), so that sequence's out
@@ -199,7 +211,7 @@ int pkv_paged_attn_decode(const pkv_shape* shape, const void* q,
  *   other arguments as pkv_paged_attn_decode; k_cache and v_cache are written
  * The block that receives a sequence's new token must not be referenced by
  * another sequence of the batch (copy it first when a prefix block is shared).
- * Runs under every schedule (split_tokens as for pkv_paged_attn_decode).
+ * Runs on every kernel variant (split_tokens as for pkv_paged_attn_decode).
  */
 int pkv_decode_step(const pkv_shape* shape, const void* q, const void* k_new,
                     const void* v_new, void* k_cache, void* v_cache,

@@ -63,6 +63,8 @@ def load_library(path: str | None = None):
     sp = ctypes.POINTER(Shape)
     lib.pkv_kv_cache_append.argtypes = [sp, vp, vp, vp, i32, vp, vp, vp]
     lib.pkv_kv_cache_append.restype = ctypes.c_int
+    lib.pkv_set_workspace.argtypes = [vp, sz]
+    lib.pkv_set_workspace.restype = ctypes.c_int
     lib.pkv_paged_attn_decode.argtypes = [sp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.pkv_paged_attn_decode.restype = ctypes.c_int
     lib.pkv_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
@@ -121,9 +123,31 @@ def strerror(code: int) -> str:
         return "libpkv not loaded"
 
 
-def _stream_ptr(stream) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return int(s.cuda_stream)
+def _stream_ptr(stream, device=None) -> int:
+    """The stream handle to launch on: `stream`, or the current stream of
+    `device` (of the current device when None)."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return int(stream.cuda_stream)
+
+
+def _one_device(**tensors) -> torch.device:
+    """The CUDA device every given tensor lives on (None entries skipped).
+    The library launches on the current device with that device's TMA
+    descriptors, so tensors of another GPU must never reach it."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, expected {dev} like the other tensors")
+    return dev
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -169,10 +193,12 @@ def kv_cache_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor
         raise ValueError("slot_mapping must be [T]")
     shape = make_shape(num_kv_heads=Hkv, head_dim=D, block_size=bs, num_blocks=NB,
                        dtype=_DT[k_cache.dtype])
+    dev = _one_device(k=k, v=v, slot_mapping=slot_mapping, k_cache=k_cache, v_cache=v_cache)
     lib = load_library()
-    _check("pkv_kv_cache_append",
-           lib.pkv_kv_cache_append(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(slot_mapping), T,
-                                   _ptr(k_cache), _ptr(v_cache), _stream_ptr(stream)))
+    with torch.cuda.device(dev):
+        _check("pkv_kv_cache_append",
+               lib.pkv_kv_cache_append(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                       T, _ptr(k_cache), _ptr(v_cache), _stream_ptr(stream, dev)))
 
 
 def decode_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
@@ -208,10 +234,46 @@ def workspace_bytes(shape: Shape) -> int:
 
 
 def alloc_workspace(shape: Shape, device=None) -> torch.Tensor | None:
-    n = workspace_bytes(shape)
+    """A workspace tensor for `shape` on `device` (None when none is needed).
+    The size is planned on that device."""
+    dev = torch.device(device or "cuda")
+    with torch.cuda.device(dev):
+        n = workspace_bytes(shape)
     if n == 0:
         return None
-    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device or "cuda")
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=dev)
+
+
+# Workspaces set with set_workspace, by device index (kept alive here).
+_SET_WS: dict[int, torch.Tensor] = {}
+
+
+def set_workspace(workspace: torch.Tensor | None, device=None) -> None:
+    """Make `workspace` (a contiguous CUDA tensor) the workspace that decode
+    calls on its device use when they are given none (pkv_set_workspace);
+    None clears the setting of `device` (default: the current device)."""
+    lib = load_library()
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        with torch.cuda.device(dev):
+            _check("pkv_set_workspace", lib.pkv_set_workspace(None, 0))
+        _SET_WS.pop(dev.index, None)
+        return
+    _dense(workspace, "workspace")
+    with torch.cuda.device(workspace.device):
+        _check("pkv_set_workspace", lib.pkv_set_workspace(_ptr(workspace), _nbytes(workspace)))
+    _SET_WS[workspace.device.index] = workspace
+
+
+def _workspace_for(shape: Shape, dev: torch.device, workspace):
+    """The workspace tensor to pass: the given one, none when a workspace is
+    set for `dev` (the library then uses that one), else a new one."""
+    if workspace is not None:
+        _dense(workspace, "workspace")
+        return workspace
+    if dev.index in _SET_WS:
+        return None
+    return alloc_workspace(shape, dev)
 
 
 def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -224,8 +286,11 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
 
     q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables [B, MB] int32;
     context_lens [B] int32.  Returns out [B, Hq, D] (allocated if not given).
-    split_tokens: 0 = library's choice, > 0 = partition size, -1 = persistent
-    schedule.  kernel: 0 = library's choice, 1 CUDA cores, 2 mma.sync, 3 tcgen05.
+    split_tokens: 0 = library's choice, > 0 = tokens per split-KV partition.
+    kernel: 0 = library's choice, 1 CUDA cores, 2 mma.sync, 3 tcgen05.
+    workspace: the split-KV scratch.  None uses the one set with
+    set_workspace for q's device, else allocates one of the planned size;
+    pass or set one to keep allocation off the decode path.
     """
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _dense(t, n, q.dtype)
@@ -238,17 +303,17 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _dense(out, "out", q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape [B, Hq, D]")
+    dev = _one_device(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                      context_lens=context_lens, out=out, workspace=workspace)
     shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens, kernel)
-    if workspace is None:
-        workspace = alloc_workspace(shape, q.device)
-    else:
-        _dense(workspace, "workspace")
+    workspace = _workspace_for(shape, dev, workspace)
     lib = load_library()
-    _check("pkv_paged_attn_decode",
-           lib.pkv_paged_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                     _ptr(block_tables), _ptr(context_lens), float(scale),
-                                     _ptr(out), _ptr(workspace), _nbytes(workspace),
-                                     _stream_ptr(stream)))
+    with torch.cuda.device(dev):
+        _check("pkv_paged_attn_decode",
+               lib.pkv_paged_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+                                         float(scale), _ptr(out), _ptr(workspace),
+                                         _nbytes(workspace), _stream_ptr(stream, dev)))
     return out
 
 
@@ -291,17 +356,18 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         _dense(out, "out", q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape [B, Hq, D]")
+    dev = _one_device(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                      block_tables=block_tables, context_lens=context_lens, out=out,
+                      workspace=workspace)
     shape = decode_shape(q, k_cache, block_tables, max_context_len, split_tokens, kernel)
-    if workspace is None:
-        workspace = alloc_workspace(shape, q.device)
-    else:
-        _dense(workspace, "workspace")
-    _check("pkv_decode_step",
-           load_library().pkv_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k_new), _ptr(v_new),
-                                          _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                          _ptr(context_lens), float(scale), _ptr(out),
-                                          _ptr(workspace), _nbytes(workspace),
-                                          _stream_ptr(stream)))
+    workspace = _workspace_for(shape, dev, workspace)
+    with torch.cuda.device(dev):
+        _check("pkv_decode_step",
+               load_library().pkv_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k_new),
+                                              _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                              _ptr(block_tables), _ptr(context_lens),
+                                              float(scale), _ptr(out), _ptr(workspace),
+                                              _nbytes(workspace), _stream_ptr(stream, dev)))
     return out
 
 
@@ -324,10 +390,15 @@ def copy_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
     _, Hkv, bs, D = src_k.shape
     shape = make_shape(num_kv_heads=Hkv, head_dim=D, block_size=bs, num_blocks=src_k.shape[0],
                        dtype=_DT[src_k.dtype])
-    _check("pkv_copy_blocks",
-           load_library().pkv_copy_blocks(ctypes.byref(shape), _ptr(src_k), _ptr(src_v),
-                                          src_k.shape[0], _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
-                                          _ptr(pairs), pairs.shape[0], _stream_ptr(stream)))
+    on_gpu = {n: t for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k),
+                                ("dst_v", dst_v), ("pairs", pairs)) if t.is_cuda}
+    dev = _one_device(**on_gpu) if on_gpu else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _check("pkv_copy_blocks",
+               load_library().pkv_copy_blocks(ctypes.byref(shape), _ptr(src_k), _ptr(src_v),
+                                              src_k.shape[0], _ptr(dst_k), _ptr(dst_v),
+                                              dst_k.shape[0], _ptr(pairs), pairs.shape[0],
+                                              _stream_ptr(stream, dev)))
 
 
 class BlockManager:

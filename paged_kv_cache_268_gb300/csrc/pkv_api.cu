@@ -4,7 +4,6 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -144,59 +143,14 @@ cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
   }
 }
 
-template <bool BF>
-cudaError_t launch_merge(const DecodeArgs& a, int D, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>((a.B * a.Hq + 7) / 8);
-  const float* po = a.part_o;
-  const float2* pml = a.part_ml;
-  const int* hdr = a.hdr;
-  switch (D) {
-    case 64:
-      return launch_dependent(persistent_merge_kernel<BF, 64>, grid, stream, po, pml, hdr, a.out,
-                              a.B, a.Hq, a.Hkv);
-    case 128:
-      return launch_dependent(persistent_merge_kernel<BF, 128>, grid, stream, po, pml, hdr, a.out,
-                              a.B, a.Hq, a.Hkv);
-    case 256:
-      return launch_dependent(persistent_merge_kernel<BF, 256>, grid, stream, po, pml, hdr, a.out,
-                              a.B, a.Hq, a.Hkv);
-    default:
-      return cudaErrorInvalidValue;
-  }
-}
-
-// Persistent schedule: phase-1 CTAs (two per SM, resident from the start) and
-// phase-2 CTAs (dispatched as SMs free up).  Workspace: header (four int64
-// then cum[0..B]), then the (max, sum) pairs and the outputs of two partial
-// slots per warp of the grid.
-constexpr int kPersistCtasPerSm = 2;
-
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-size_t persist_hdr_bytes(int B) { return round_up((9 + static_cast<size_t>(B)) * 4, 256); }
-
-// Tuning overrides, read once: share of the blocks streamed by phase 1 (per
-// mille, default 750) and phase-2 CTAs per SM (default 4).
-int env_int(const char* name, int dflt, int lo, int hi) {
-  const char* v = getenv(name);
-  if (!v || !*v) return dflt;
-  const long x = strtol(v, nullptr, 10);
-  return x < lo ? lo : (x > hi ? hi : static_cast<int>(x));
-}
-int phase1_per_mille() {
-  static const int v = env_int("PKV_PHASE1_PERMILLE", 750, 0, 1000);
-  return v;
-}
-int phase2_ctas_per_sm() {
-  static const int v = env_int("PKV_PHASE2_CTAS_PER_SM", 4, 0, 64);
-  return v;
-}
-
 // ------------------------------------------------------------------ devices
 struct DeviceInfo {
   bool valid = false;
   int sms = 0;
   int* err = nullptr;
+  // workspace set with pkv_set_workspace (caller-owned; null when none)
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
 };
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[64];
@@ -307,7 +261,7 @@ int check_decode_shape(const pkv_shape* s) {
   int rc = check_cache_shape(s);
   if (rc != PKV_OK) return rc;
   if (s->num_seqs < 0 || s->num_q_heads < 1 || s->max_blocks_per_seq < 1 ||
-      s->max_context_len < 1 || s->split_tokens < -1 || s->kernel < 0 || s->kernel > 3)
+      s->max_context_len < 1 || s->split_tokens < 0 || s->kernel < 0 || s->kernel > 3)
     return PKV_ERR_INVALID;
   if (s->num_q_heads % s->num_kv_heads != 0) return PKV_ERR_INVALID;
   if (static_cast<long long>(s->max_context_len) >
@@ -319,11 +273,11 @@ int check_decode_shape(const pkv_shape* s) {
 }
 
 // Inner-loop variant (0 CUDA cores, 1 mma.sync, 2 tcgen05) for a shape, or -1
-// when the requested one cannot run it.  The tcgen05 kernel serves the
-// partition schedule (plain decode or fused step).
+// when the requested one cannot run it.  Every variant serves the plain
+// decode and the fused step.
 int pick_variant(const pkv_shape* s) {
   const int G = s->num_q_heads / s->num_kv_heads;
-  const bool tc_ok = s->head_dim == 128 && G <= 32 && s->split_tokens != -1;
+  const bool tc_ok = s->head_dim == 128 && G <= 32;
   switch (s->kernel) {
     case 1: return G <= 2 ? 0 : -1;
     case 2: return 1;
@@ -352,21 +306,6 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   plan->warps_per_cta = geo.warps;
   plan->stages_per_warp = geo.stages;
   const long long units = static_cast<long long>(s->num_seqs) * s->num_kv_heads;
-  const bool persist_ok =
-      s->num_seqs <= kPersistMaxSeqs &&
-      static_cast<long long>(s->num_seqs) * s->max_blocks_per_seq * s->num_kv_heads < (1ll << 31);
-  if (s->split_tokens == -1 && persist_ok) {
-    plan->schedule = 1;
-    plan->split_tokens = 0;
-    plan->num_splits = 0;
-    const int f = phase1_per_mille();
-    const int g2 = f == 1000 ? 0 : sms * phase2_ctas_per_sm();
-    plan->grid_ctas = sms * kPersistCtasPerSm + g2;
-    const size_t W = static_cast<size_t>(plan->grid_ctas) * geo.warps;
-    plan->workspace_bytes = persist_hdr_bytes(s->num_seqs) + 2 * W * G * 8 +
-                            2 * W * G * static_cast<size_t>(s->head_dim) * 4;
-    return PKV_OK;
-  }
   plan->schedule = 0;
   const int maxL = s->max_context_len;
   // every warp gets the same block count; the tcgen05 kernel walks 128-token groups
@@ -429,6 +368,13 @@ bool decode_geometry(int D, int BS, int variant, int G, KernelGeometry* g) {
   return true;
 }
 
+// The workspace set for the current device, or {nullptr, 0}.
+static void set_workspace_of(DeviceInfo* d, void** ptr, size_t* bytes) {
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  *ptr = d->ws;
+  *bytes = d->ws_bytes;
+}
+
 int* device_error_word() {
   DeviceInfo* d = nullptr;
   return current_device(&d) == PKV_OK ? d->err : nullptr;
@@ -484,6 +430,32 @@ extern "C" int pkv_workspace_bytes(const pkv_shape* s, size_t* bytes) {
   return PKV_OK;
 }
 
+extern "C" int pkv_set_workspace(void* dev_ptr, size_t bytes) {
+  if (dev_ptr != nullptr) {
+    if (bytes == 0) return PKV_ERR_INVALID;
+    if (!aligned(dev_ptr, 16)) return PKV_ERR_ALIGN;
+  }
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != PKV_OK) return rc;
+  if (dev_ptr != nullptr) {
+    // it must be memory of the current device (not host memory, not another GPU's)
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, dev_ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_INVALID;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != dev)
+      return PKV_ERR_INVALID;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  d->ws = dev_ptr;
+  d->ws_bytes = dev_ptr ? bytes : 0;
+  return PKV_OK;
+}
+
 extern "C" int pkv_kv_cache_append(const pkv_shape* s, const void* k, const void* v,
                                    const int32_t* slot_mapping, int32_t num_tokens,
                                    void* k_cache, void* v_cache, pkv_stream_t stream) {
@@ -530,6 +502,7 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   rc = make_plan(s, d->sms, &plan);
   if (rc != PKV_OK) return rc;
   if (plan.workspace_bytes > 0) {
+    if (!workspace) set_workspace_of(d, &workspace, &workspace_bytes);
     if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16))
       return PKV_ERR_WORKSPACE;
   }
@@ -547,13 +520,7 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   a.context_lens = context_lens;
   a.out = static_cast<uint16_t*>(out);
   const int G = s->num_q_heads / s->num_kv_heads;
-  if (plan.schedule == 1) {
-    uint8_t* w = static_cast<uint8_t*>(workspace);
-    const size_t W = static_cast<size_t>(plan.grid_ctas) * plan.warps_per_cta;
-    a.hdr = reinterpret_cast<int*>(w);
-    a.part_ml = reinterpret_cast<float2*>(w + persist_hdr_bytes(s->num_seqs));
-    a.part_o = reinterpret_cast<float*>(a.part_ml + 2 * W * G);
-  } else {
+  {
     const size_t rows = static_cast<size_t>(s->num_seqs) * s->num_q_heads * plan.num_splits;
     a.part_o = plan.workspace_bytes ? static_cast<float*>(workspace) : nullptr;
     a.part_ml = plan.workspace_bytes ? reinterpret_cast<float2*>(static_cast<float*>(workspace) +
@@ -575,28 +542,22 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   a.P = plan.split_tokens;
   a.max_ctx = s->max_context_len;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-  a.g1 = d->sms * kPersistCtasPerSm;
-  a.f_per_mille = plan.grid_ctas > a.g1 ? phase1_per_mille() : 1000;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = s->dtype == PKV_BF16;
-  const int D = s->head_dim, BS = s->block_size, sc = plan.schedule, grid = plan.grid_ctas;
+  const int D = s->head_dim, BS = s->block_size;
   cudaError_t e;
   if (plan.variant == 2)
     e = launch_decode_tc(a, tk, tv, bf, D, BS, st);
   else if (plan.variant == 0)
-    e = bf ? launch_decode_bf16_simt(a, tk, tv, D, BS, sc, grid, st)
-           : launch_decode_f16_simt(a, tk, tv, D, BS, sc, grid, st);
+    e = bf ? launch_decode_bf16_simt(a, tk, tv, D, BS, st)
+           : launch_decode_f16_simt(a, tk, tv, D, BS, st);
   else
-    e = bf ? launch_decode_bf16_mma(a, tk, tv, D, BS, sc, grid, st)
-           : launch_decode_f16_mma(a, tk, tv, D, BS, sc, grid, st);
+    e = bf ? launch_decode_bf16_mma(a, tk, tv, D, BS, st)
+           : launch_decode_f16_mma(a, tk, tv, D, BS, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   g_launches.fetch_add(1);
-  if (plan.schedule == 1) {
-    e = bf ? launch_merge<true>(a, D, st) : launch_merge<false>(a, D, st);
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
-    g_launches.fetch_add(1);
-  } else if (plan.num_splits > 1) {
+  if (plan.num_splits > 1) {
     e = bf ? launch_reduce<true>(a, D, st) : launch_reduce<false>(a, D, st);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     g_launches.fetch_add(1);

@@ -95,29 +95,6 @@ struct SimtCompute {
     }
   }
 
-  // Write this warp's result for the group straight from registers: the
-  // normalised rows (out_rows, GH rows of D) when the warp saw the whole
-  // context, else the un-normalised partial (po: GH rows of D floats,
-  // pml: GH (max, sum) pairs).
-  __device__ __forceinline__ void finish(bool final_rows, uint16_t* out_rows, float* po,
-                                         float2* pml, int /*G*/, int lane) {
-#pragma unroll
-    for (int gh = 0; gh < GH; ++gh) {
-      float lt = l[gh];
-      lt += __shfl_xor_sync(kFull, lt, 1);
-      lt += __shfl_xor_sync(kFull, lt, 2);
-      lt += __shfl_xor_sync(kFull, lt, 4);
-      if (final_rows) {
-#pragma unroll
-        for (int e = 0; e < OPL; ++e) out_rows[gh * D + lane * OPL + e] = to_elem<BF>(o[gh][e] / lt);
-      } else {
-#pragma unroll
-        for (int e = 0; e < OPL; ++e) po[gh * D + lane * OPL + e] = o[gh][e];
-        if (lane == 0) pml[gh] = make_float2(m[gh], lt);
-      }
-    }
-  }
-
   __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float scale_log2,
                                         int lane) {
     const int t8 = lane & 7, dq = lane >> 3;
@@ -402,41 +379,6 @@ struct MmaCompute {
         }
     }
   }
-
-  // As SimtCompute::finish, for the G real heads of the tiles.
-  __device__ __forceinline__ void finish(bool final_rows, uint16_t* out_rows, float* po,
-                                         float2* pml, int G, int lane) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float lt[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float v = l[nt][j];
-        v += __shfl_xor_sync(kFull, v, 4);
-        v += __shfl_xor_sync(kFull, v, 8);
-        v += __shfl_xor_sync(kFull, v, 16);
-        lt[j] = v;
-      }
-#pragma unroll
-      for (int dt = 0; dt < KS; ++dt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int d = dt * 16 + (lane >> 2) + ((e >> 1) << 3);
-          const int h = nt * 8 + 2 * (lane & 3) + (e & 1);
-          if (h < G) {
-            if (final_rows)
-              out_rows[h * D + d] = to_elem<BF>(o[dt][nt][e] / lt[e & 1]);
-            else
-              po[h * D + d] = o[dt][nt][e];
-          }
-        }
-      if (!final_rows && lane < 4) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          if (nt * 8 + 2 * lane + j < G) pml[nt * 8 + 2 * lane + j] = make_float2(m[nt][j], lt[j]);
-      }
-    }
-  }
 };
 
 // ------------------------------------------------------------------ kernel
@@ -573,10 +515,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int kk = k; kk < hi; ++kk) mbar_wait(wbar + 8 * (kk % NS), (kk / NS) & 1, 100000000ull);
     if (lane == 0) record_error(a.err, kDevTimeout);
   }
+  // A wait that gave up fails the whole CTA: it writes no result (the merge
+  // below would reuse a stage ring that a late load may still be filling).
+  if (__syncthreads_or(!ok)) return;
 
   // Merge the warps' (m, l, o) through shared memory (the stage ring is free:
-  // every issued load has been consumed).
-  __syncthreads();
+  // on this path every warp consumed every load it issued).
   float* cm = reinterpret_cast<float*>(smem);
   float* cl = cm + NW * NH;
   float* co = cl + NW * NH;
@@ -608,361 +552,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
-// ------------------------------------------------------------------ persistent
-// Stream-K schedule.  The blocks of every (sequence, kv head) unit are laid
-// end to end in one list, ordered by kv head, then sequence, then logical
-// block: unit (i, h) owns list entries h*cum[B] + cum[i] + j, j < nblk_i,
-// where nblk_i = ceil(L_i / bs) and cum is its exclusive prefix sum; T =
-// Hkv*cum[B] is the list length.  Head-major order lines the warps of
-// different heads up on the same (sequence, block) positions, so warps that
-// run side by side read neighbouring tiles of one physical block.  The list is cut into warp ranges in two phases:
-//   phase 1: the first T1 = T * f entries go to the warps of the first
-//            `g1` CTAs (2 per SM, resident from the start) in W1 equal
-//            contiguous ranges, so those warps stream without a break;
-//   phase 2: the remaining entries go to the warps of the later CTAs in
-//            equal chunks of C2; the hardware dispatches those CTAs to
-//            whichever SMs finish phase 1 first, which absorbs the SMs'
-//            unequal memory bandwidth.
-// Range boundaries depend only on the lengths, never on timing, so results
-// are deterministic.  Ranges are numbered 0..W1-1 (phase 1), then W1.. (phase
-// 2); range x covers [a(x), a(x+1)).  A unit wholly inside one range is
-// written out normalised; a unit cut by range boundaries leaves one partial
-// per range that touched it (slot 2x for the range's first unit, 2x+1 for its
-// last), merged by persistent_merge_kernel.
-
-struct StreamK {
-  long long T, T1, W1, C2;
-  __device__ __forceinline__ long long range_start(long long x) const {
-    if (x < W1) return x * T1 / W1;
-    const long long v = T1 + (x - W1) * C2;
-    return v < T ? v : T;
-  }
-  // index of the range that holds list entry n (0 <= n < T)
-  __device__ __forceinline__ long long range_of(long long n) const {
-    if (n < T1) return ((n + 1) * W1 - 1) / T1;
-    return W1 + (n - T1) / C2;
-  }
-};
-
-// Phase split shared by every CTA and by the merge kernel.
-__device__ __forceinline__ StreamK make_streamk(long long T, int g1_warps, int g2_warps,
-                                                int f_per_mille) {
-  StreamK sk;
-  sk.T = T;
-  if (g2_warps == 0) f_per_mille = 1000;
-  sk.T1 = T * f_per_mille / 1000;
-  sk.W1 = sk.T1 == 0 ? 0 : min((long long)g1_warps, max(1ll, sk.T1 / 4));
-  if (sk.W1 == 0) sk.T1 = 0;
-  const long long rest = T - sk.T1;
-  sk.C2 = (rest == 0 || g2_warps == 0) ? 1 : (rest + g2_warps - 1) / g2_warps;
-  return sk;
-}
-
-// Exclusive prefix of per-sequence block counts into cum[0..B] (shared),
-// using every thread of the CTA.
-template <int BS, int NT>
-__device__ __forceinline__ void block_prefix(const int32_t* lens, int B, int max_ctx, int* cum,
-                                             int* warp_tot, int* err, bool report) {
-  const int tid = threadIdx.x;
-  const int per = (B + NT - 1) / NT;
-  const int lo = min(tid * per, B), hi = min(lo + per, B);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) {
-    const int L = lens[i];
-    const bool ok = L >= 1 && L <= max_ctx;
-    if (!ok && report) record_error(err, kDevBadContext);
-    const int nb = ok ? (L + BS - 1) / BS : 0;
-    cum[i + 1] = nb;
-    sum += nb;
-  }
-  // block-wide exclusive scan of the per-thread sums
-  const int lane = tid & 31, wid = tid >> 5;
-  int inc = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, inc, o);
-    if (lane >= o) inc += y;
-  }
-  if (lane == 31) warp_tot[wid] = inc;
-  __syncthreads();
-  int base = 0;
-  for (int w = 0; w < wid; ++w) base += warp_tot[w];
-  int run = base + inc - sum;
-  for (int i = lo; i < hi; ++i) {
-    run += cum[i + 1];
-    cum[i + 1] = run;
-  }
-  if (tid == 0) cum[0] = 0;
-  __syncthreads();
-}
-
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-template <bool BF, int D, int BS, int NW, int NS, class Compute>
-__global__ void __launch_bounds__(NW * 32, 1)
-    paged_decode_persistent(const __grid_constant__ DecodeArgs a,
-                            const __grid_constant__ CUtensorMap tmK,
-                            const __grid_constant__ CUtensorMap tmV) {
-  constexpr int TILE = BS * D * 2;
-  constexpr int STAGE = 2 * TILE;
-  constexpr int CH = D / 64;
-  __shared__ int warp_tot[NW];
-  // per warp: two windows of 32 list entries (physical id, unit, block)
-  __shared__ int win[NW][2][3][32];
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NS * STAGE);
-  int2* smeta = reinterpret_cast<int2*>(bars + NW * NS);
-  int* cum = reinterpret_cast<int*>(smeta + NW * NS);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = a.B, Hkv = a.Hkv;
-  pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-  }
-  if (threadIdx.x < NW * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
-  if (threadIdx.x == 0) fence_mbar_init();
-  block_prefix<BS, NW * 32>(a.context_lens, B, a.max_ctx, cum, warp_tot, a.err, blockIdx.x == 0);
-
-  const int Tseq = cum[B];  // blocks per kv head
-  const StreamK sk = make_streamk((long long)Hkv * Tseq, a.g1 * NW,
-                                  (int)(gridDim.x - a.g1) * NW, a.f_per_mille);
-  if (blockIdx.x == 0) {
-    // schedule header for the merge kernel
-    for (int i = threadIdx.x; i <= B; i += NW * 32) a.hdr[8 + i] = cum[i];
-    if (threadIdx.x == 0) {
-      reinterpret_cast<long long*>(a.hdr)[0] = sk.T;
-      reinterpret_cast<long long*>(a.hdr)[1] = sk.T1;
-      reinterpret_cast<long long*>(a.hdr)[2] = sk.W1;
-      reinterpret_cast<long long*>(a.hdr)[3] = sk.C2;
-    }
-  }
-  long long x;  // this warp's range index
-  if ((int)blockIdx.x < a.g1) {
-    x = (long long)blockIdx.x * NW + warp;
-    if (x >= sk.W1) return;
-  } else {
-    x = sk.W1 + (long long)(blockIdx.x - a.g1) * NW + warp;
-  }
-  const long long r0 = sk.range_start(x);
-  const long long nb = sk.range_start(x + 1) - r0;
-  if (nb <= 0) return;
-
-  // Resolve list entries base .. base+31 of this range into window `buf`:
-  // binary search over cum for the sequence, then an asynchronous 4-byte copy
-  // of the block-table entry straight into shared memory.
-  int(*wn)[3][32] = win[warp];
-  auto load_win = [&](long long base, int buf) {
-    const long long rel = base + lane;
-    int u = 0, j = 0;
-    if (rel < nb) {
-      const long long n = r0 + rel;
-      const int h = static_cast<int>(n / Tseq);
-      const int m = static_cast<int>(n - (long long)h * Tseq);
-      int lo = 0, hi = B;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cum[mid] <= m) lo = mid; else hi = mid;
-      }
-      j = m - cum[lo];
-      u = lo * Hkv + h;
-      cp_async_4(smem_u32(&wn[buf][0][lane]), a.block_tables + (size_t)lo * a.MB + j);
-    }
-    wn[buf][1][lane] = u;
-    wn[buf][2][lane] = j;
-    cp_async_commit();
-  };
-  load_win(0, 0);
-  load_win(32, 1);
-  cp_async_wait_all();
-  __syncwarp();
-
-  const uint32_t wbuf = smem_u32(smem + warp * NS * STAGE);
-  const uint32_t wbar = smem_u32(&bars[warp * NS]);
-  int2* wmeta = smeta + warp * NS;
-
-  // lane 0 only
-  auto issue = [&](long long p) {
-    const int buf = static_cast<int>((p >> 5) & 1), e = static_cast<int>(p & 31);
-    int id = wn[buf][0][e];
-    const int u = wn[buf][1][e];
-    if (id < 0 || id >= a.NB) {
-      record_error(a.err, kDevBadBlock);
-      id = 0;
-    }
-    const int st = static_cast<int>(p % NS);
-    wmeta[st] = make_int2(u, wn[buf][2][e]);
-    const int kvh = u - (u / Hkv) * Hkv;
-    const int y = (id * Hkv + kvh) * BS;
-    const uint32_t bar = wbar + 8 * st;
-    const uint32_t dk = wbuf + st * STAGE;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      tma_load_2d(dk + c * BS * 128, &tmK, c * 64, y, bar);
-      tma_load_2d(dk + TILE + c * BS * 128, &tmV, c * 64, y, bar);
-    }
-  };
-  if (lane == 0) {
-    const long long pro = nb < NS ? nb : NS;
-    for (long long p = 0; p < pro; ++p) issue(p);
-  }
-
-  Compute cs;
-  int cur_u = -1, first_j = 0, last_j = 0, cur_L = 0, part = 0;
-  auto finish = [&](int u, int fj, int lj, int k) {
-    const int i = u / Hkv, h = u - i * Hkv;
-    const int nbk = cum[i + 1] - cum[i];
-    const size_t row0 = (size_t)i * a.Hq + (size_t)h * a.G;
-    const size_t slot = (size_t)x * 2 + k;
-    cs.finish(fj == 0 && lj == nbk - 1, a.out + row0 * D, a.part_o + slot * a.G * D,
-              a.part_ml + slot * a.G, a.G, lane);
-  };
-
-  long long r = 0;
-  bool ok = true;
-  for (; r < nb; ++r) {
-    const int st = static_cast<int>(r % NS);
-    const bool done = mbar_wait(wbar + 8 * st, static_cast<uint32_t>((r / NS) & 1));
-    if (!__all_sync(kFull, done)) { ok = false; break; }
-    const int2 mt = wmeta[st];
-    if (mt.x != cur_u) {
-      if (cur_u >= 0) {
-        finish(cur_u, first_j, last_j, part);
-        part = 1;
-      }
-      cur_u = mt.x;
-      first_j = mt.y;
-      const int i = cur_u / Hkv, h = cur_u - i * Hkv;
-      cur_L = a.context_lens[i];
-      cs.load_q(a.q + ((size_t)i * a.Hq + (size_t)h * a.G) * D, a.G, lane);
-      cs.reset();
-    }
-    last_j = mt.y;
-    const uint32_t kt = wbuf + st * STAGE;
-    if (a.k_new != nullptr && mt.y == (cur_L - 1) / BS) {
-      // Fused append: this step's token (position L-1) goes to its slot in
-      // the cache and into the staged tile (as in the partition kernel).
-      const int i = cur_u / Hkv, h = cur_u - i * Hkv;
-      const int pid = a.block_tables[(size_t)i * a.MB + mt.y];
-      const int rr = (cur_L - 1) - mt.y * BS;
-      const size_t src = ((size_t)i * Hkv + h) * D;
-      const size_t dst = (((size_t)pid * Hkv + h) * BS + rr) * D;
-      const bool in_pool = pid >= 0 && pid < a.NB;   // a bad id was reported at issue
-      for (int c = lane; c < 2 * (D / 8); c += 32) {
-        const bool isv = c >= D / 8;
-        const int gc = isv ? c - D / 8 : c;
-        const uint4 xv =
-            *reinterpret_cast<const uint4*>((isv ? a.v_new : a.k_new) + src + gc * 8);
-        const uint32_t sa = (isv ? kt + TILE : kt) + tile_off<BS>(rr, gc);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sa), "r"(xv.x), "r"(xv.y),
-                     "r"(xv.z), "r"(xv.w)
-                     : "memory");
-        if (in_pool)
-          *reinterpret_cast<uint4*>((isv ? a.v_cache : a.k_cache) + dst + gc * 8) = xv;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-    cs.block(kt, kt + TILE, min(BS, cur_L - mt.y * BS), a.scale_log2, lane);
-    __syncwarp();
-    const long long p = r + NS;
-    if (p < nb) {
-      if ((p & 31) == 0) {
-        // the producer enters window p/32 (landed long ago); refill the
-        // window it just left with the one after
-        cp_async_wait_all();
-        __syncwarp();
-        load_win(p + 32, static_cast<int>(((p >> 5) + 1) & 1));
-      }
-      if (lane == 0) issue(p);
-    }
-  }
-  if (!ok) {
-    const long long hi = min(r + NS, nb);
-    for (long long kk = r; kk < hi; ++kk)
-      mbar_wait(wbar + 8 * static_cast<int>(kk % NS), static_cast<uint32_t>((kk / NS) & 1),
-                100000000ull);
-    cp_async_wait_all();
-    if (lane == 0) record_error(a.err, kDevTimeout);
-    return;
-  }
-  cp_async_wait_all();
-  if (cur_u >= 0) finish(cur_u, first_j, last_j, part);
-}
-
-// Merge of the units that range boundaries cut: one warp per (sequence,
-// query head).  The ranges that touched unit u are range_of(s_u) ..
-// range_of(e_u - 1); each left one partial, merged in range order
-// (deterministic).
-template <bool BF, int D>
-__global__ void __launch_bounds__(256)
-    persistent_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                            const int* __restrict__ hdr, uint16_t* __restrict__ out, int B,
-                            int Hq, int Hkv) {
-  constexpr int OPL = D / 32;
-  pdl_wait();
-  const int gq = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gq >= B * Hq) return;
-  const int G = Hq / Hkv;
-  const int i = gq / Hq, hq = gq - i * Hq, h = hq / G, g = hq - h * G;
-  const long long* h64 = reinterpret_cast<const long long*>(hdr);
-  StreamK sk;
-  sk.T = h64[0];
-  sk.T1 = h64[1];
-  sk.W1 = h64[2];
-  sk.C2 = h64[3];
-  if (sk.T == 0) return;
-  const int* cum = hdr + 8;
-  const int nbk = cum[i + 1] - cum[i];
-  if (nbk == 0) return;
-  const long long s = (long long)h * cum[B] + cum[i];
-  const long long e = s + nbk;
-  const long long xs = sk.range_of(s);
-  const long long xe = sk.range_of(e - 1);
-  if (xs == xe) return;  // one range held the whole unit and wrote it out
-  const bool first_is_tail = s != sk.range_start(xs);
-  auto slot = [&](long long x) { return x * 2 + ((x == xs && first_is_tail) ? 1 : 0); };
-  float M = -INFINITY;
-  for (long long x = xs + lane; x <= xe; x += 32) M = fmaxf(M, part_ml[slot(x) * G + g].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  float lsum = 0.f;
-  for (long long x = xs + lane; x <= xe; x += 32) {
-    const float2 ml = part_ml[slot(x) * G + g];
-    lsum = fmaf(fast_exp2(ml.x - M), ml.y, lsum);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
-  float acc[OPL];
-#pragma unroll
-  for (int k = 0; k < OPL; ++k) acc[k] = 0.f;
-  for (long long x = xs; x <= xe; ++x) {
-    const long long sl = slot(x);
-    const float wt = fast_exp2(part_ml[sl * G + g].x - M);
-    const float* po = part_o + (sl * G + g) * D + lane * OPL;
-#pragma unroll
-    for (int k = 0; k < OPL; ++k) acc[k] = fmaf(wt, po[k], acc[k]);
-  }
-  uint16_t* orow = out + ((size_t)i * Hq + hq) * D + lane * OPL;
-#pragma unroll
-  for (int k = 0; k < OPL; ++k) orow[k] = to_elem<BF>(acc[k] / lsum);
-}
-
+// ------------------------------------------------------------------ reduce
 // Cross-split reduce: one warp per (sequence, query head) with more than one
 // split.  M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
 // summed in split order (deterministic).  Lane j holds (m, l) of split j (of

@@ -35,20 +35,8 @@ cudaError_t configure(K kern, int smem, std::atomic<unsigned>* mask) {
 
 template <int D, int BS, class Compute>
 cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                       int schedule, int grid, cudaStream_t stream) {
+                       cudaStream_t stream) {
   constexpr int NW = geo_warps(D, BS);
-  if (schedule == 1) {
-    constexpr int NS = geo_stages(D, BS);
-    constexpr int SMEM_MAX = geo_persist_smem(D, BS, kPersistMaxSeqs);
-    static_assert(SMEM_MAX <= 113 * 1024, "two persistent CTAs must fit on one SM");
-    static_assert(ctas_per_sm_for(SMEM_MAX) >= 2, "two persistent CTAs must fit on one SM");
-    auto kern = paged_decode_persistent<kBF, D, BS, NW, NS, Compute>;
-    static std::atomic<unsigned> mask{0};
-    cudaError_t e = configure(kern, SMEM_MAX, &mask);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, NW * 32, geo_persist_smem(D, BS, a.B), stream>>>(a, tk, tv);
-    return cudaGetLastError();
-  }
   constexpr int NS = part_stages(D, BS, Compute::NH);
   constexpr int SMEM = part_smem(D, BS, Compute::NH);
   auto kern = paged_decode_kernel<kBF, D, BS, NW, NS, Compute>;
@@ -73,31 +61,31 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
 
 template <int D, int BS>
 cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                           int schedule, int grid, cudaStream_t stream) {
+                           cudaStream_t stream) {
 #if PKV_INST_MMA
   if (a.G >= 1 && a.G <= 8)
-    return launch_one<D, BS, MmaCompute<kBF, D, BS, 1>>(a, tk, tv, schedule, grid, stream);
+    return launch_one<D, BS, MmaCompute<kBF, D, BS, 1>>(a, tk, tv, stream);
   if (a.G >= 9 && a.G <= 16)
-    return launch_one<D, BS, MmaCompute<kBF, D, BS, 2>>(a, tk, tv, schedule, grid, stream);
+    return launch_one<D, BS, MmaCompute<kBF, D, BS, 2>>(a, tk, tv, stream);
   if (a.G >= 17 && a.G <= 32)
-    return launch_one<D, BS, MmaCompute<kBF, D, BS, 4>>(a, tk, tv, schedule, grid, stream);
+    return launch_one<D, BS, MmaCompute<kBF, D, BS, 4>>(a, tk, tv, stream);
 #else
   if (a.G == 1)
-    return launch_one<D, BS, SimtCompute<kBF, D, BS, 1>>(a, tk, tv, schedule, grid, stream);
+    return launch_one<D, BS, SimtCompute<kBF, D, BS, 1>>(a, tk, tv, stream);
   if (a.G == 2)
-    return launch_one<D, BS, SimtCompute<kBF, D, BS, 2>>(a, tk, tv, schedule, grid, stream);
+    return launch_one<D, BS, SimtCompute<kBF, D, BS, 2>>(a, tk, tv, stream);
 #endif
   return cudaErrorInvalidValue;
 }
 
 cudaError_t dispatch(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int D,
-                     int BS, int sc, int grid, cudaStream_t stream) {
-  if (D == 64 && BS == 16) return launch_variant<64, 16>(a, tk, tv, sc, grid, stream);
-  if (D == 64 && BS == 32) return launch_variant<64, 32>(a, tk, tv, sc, grid, stream);
-  if (D == 128 && BS == 16) return launch_variant<128, 16>(a, tk, tv, sc, grid, stream);
-  if (D == 128 && BS == 32) return launch_variant<128, 32>(a, tk, tv, sc, grid, stream);
-  if (D == 256 && BS == 16) return launch_variant<256, 16>(a, tk, tv, sc, grid, stream);
-  if (D == 256 && BS == 32) return launch_variant<256, 32>(a, tk, tv, sc, grid, stream);
+                     int BS, cudaStream_t stream) {
+  if (D == 64 && BS == 16) return launch_variant<64, 16>(a, tk, tv, stream);
+  if (D == 64 && BS == 32) return launch_variant<64, 32>(a, tk, tv, stream);
+  if (D == 128 && BS == 16) return launch_variant<128, 16>(a, tk, tv, stream);
+  if (D == 128 && BS == 32) return launch_variant<128, 32>(a, tk, tv, stream);
+  if (D == 256 && BS == 16) return launch_variant<256, 16>(a, tk, tv, stream);
+  if (D == 256 && BS == 32) return launch_variant<256, 32>(a, tk, tv, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -114,9 +102,8 @@ cudaError_t dispatch(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 #endif
 
 cudaError_t PKV_LAUNCH_NAME(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                            int head_dim, int block_size, int schedule, int grid,
-                            cudaStream_t stream) {
-  return dispatch(a, tk, tv, head_dim, block_size, schedule, grid, stream);
+                            int head_dim, int block_size, cudaStream_t stream) {
+  return dispatch(a, tk, tv, head_dim, block_size, stream);
 }
 
 }  // namespace pkv

@@ -19,9 +19,6 @@ constexpr int geo_warps(int D, int BS) {
   return stage_bytes(D, BS) <= 8192 ? 4 : (stage_bytes(D, BS) <= 16384 ? 2 : 1);
 }
 
-// Stages per warp of the persistent kernel.
-constexpr int geo_stages(int /*D*/, int /*BS*/) { return 2; }
-
 // Partition kernel, per compute variant (NH = padded heads one warp
 // produces: the group for the CUDA-core variant, 8 per n-tile for mma.sync).
 // Tensor-core tiles of 16 or more heads (8 KB stages) need so many registers
@@ -46,17 +43,6 @@ constexpr int part_smem(int D, int BS, int NH) {
 // Padded heads per warp of a variant (0 CUDA cores, 1 mma.sync) for group G.
 constexpr int compute_heads(int variant, int G) {
   return variant == 0 ? G : 8 * (G <= 8 ? 1 : (G <= 16 ? 2 : 4));
-}
-
-// Largest batch the persistent schedule takes (its per-sequence block prefix
-// lives in shared memory); larger batches use the fixed-partition schedule.
-constexpr int kPersistMaxSeqs = 2048;
-
-// Persistent kernel: stage ring + mbarriers + per-stage (unit, block) tags +
-// the block prefix cum[0..B] + alignment slack.
-constexpr int geo_persist_smem(int D, int BS, int B) {
-  return geo_warps(D, BS) * geo_stages(D, BS) * stage_bytes(D, BS) +
-         geo_warps(D, BS) * geo_stages(D, BS) * 16 + (B + 1) * 4 + 1024;
 }
 
 // Resident CTAs per SM for a dynamic shared-memory size (228 KB per SM, 1 KB

@@ -20,17 +20,12 @@ struct DecodeArgs {
   const int32_t* block_tables;  // [B, MB]
   const int32_t* context_lens;  // [B]
   uint16_t* out;                // [B, Hq, D]
-  float* part_o;                // un-normalised partial outputs: [B, Hq, S, D]
-                                // (split schedule) or [2 * warps, G, D] (persistent)
+  float* part_o;                // un-normalised partial outputs [B, Hq, S, D]
   float2* part_ml;              // (running max in log2 units, sum) per partial row
-  int* hdr;                     // persistent schedule header: 4 x int64 (T, T1,
-                                // W1, C2), then cum[0..B] as int from int index 8
   const uint16_t* k_new;        // fused append: this step's K/V rows [B, Hkv, D],
   const uint16_t* v_new;        //   or null for a plain decode
   uint16_t* k_cache;            // fused append: the caches the rows go to
   uint16_t* v_cache;
-  int g1;                       // persistent: CTAs of phase 1 (the rest are phase 2)
-  int f_per_mille;              // persistent: share of the list in phase 1 (x 1/1000)
   int* err;                     // device error word
   int B, Hq, Hkv, G, MB, NB;
   int S;                        // splits per sequence (grid extent)
@@ -51,24 +46,20 @@ struct KernelGeometry {
 bool decode_geometry(int head_dim, int block_size, int variant, int group_size,
                      KernelGeometry* g);
 
-// Launch the decode kernel.  schedule 0: fixed partitions, grid B * Hkv * S;
-// schedule 1: persistent, `grid` CTAs.  Returns cudaErrorInvalidValue for an
-// unbuilt combination.
+// Launch the decode kernel over the grid B * Hkv * S of (sequence, kv head,
+// partition) units.  Returns cudaErrorInvalidValue for an unbuilt combination.
 cudaError_t launch_decode_f16_simt(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                   int head_dim, int block_size, int schedule, int grid,
-                                   cudaStream_t);
+                                   int head_dim, int block_size, cudaStream_t);
 cudaError_t launch_decode_bf16_simt(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                    int head_dim, int block_size, int schedule, int grid,
-                                    cudaStream_t);
+                                    int head_dim, int block_size, cudaStream_t);
 cudaError_t launch_decode_f16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                  int head_dim, int block_size, int schedule, int grid,
-                                  cudaStream_t);
+                                  int head_dim, int block_size, cudaStream_t);
 cudaError_t launch_decode_bf16_mma(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&,
-                                   int head_dim, int block_size, int schedule, int grid,
-                                   cudaStream_t);
+                                   int head_dim, int block_size, cudaStream_t);
 
-// tcgen05 variant (head_dim 128, group size up to 32): same grid as the
-// partition schedule, partitions a multiple of 128 tokens.
+// tcgen05 variant (head_dim 128, group size up to 32): same grid and
+// partitions as the other variants; it walks a partition in 128-token groups
+// (the last one may be ragged).
 cudaError_t launch_decode_tc(const DecodeArgs&, const CUtensorMap&, const CUtensorMap&, bool bf16,
                              int head_dim, int block_size, cudaStream_t);
 int tc_smem_bytes(int group_size);

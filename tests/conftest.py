@@ -12,6 +12,15 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 
 
+# Run last, whatever the file order: the tests of the decode entry point that
+# keeps its scratch in a library-owned device array.
+LAST = "test_zz_no_alloc.py"
+
+
+def pytest_collection_modifyitems(session, config, items):
+    items.sort(key=lambda it: os.path.basename(str(it.fspath)) == LAST)
+
+
 @pytest.fixture(scope="session")
 def oracle_lib():
     import oracle

@@ -17,8 +17,8 @@ def lib():
 def test_exports_every_declared_function(lib):
     names = B.header_functions()
     assert {"pkv_kv_cache_append", "pkv_paged_attn_decode", "pkv_workspace_bytes",
-            "pkv_decode_plan", "pkv_get_device_error", "pkv_strerror",
-            "pkv_launch_count", "pkv_version"} <= set(names)
+            "pkv_set_workspace", "pkv_decode_step", "pkv_decode_plan", "pkv_get_device_error",
+            "pkv_strerror", "pkv_launch_count", "pkv_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -53,6 +53,7 @@ def _decode(lib, shape, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE, ws
     (dict(max_context_len=0), -2),
     (dict(max_context_len=129), -2),                     # > MB * bs
     (dict(split_tokens=-2), -2),
+    (dict(split_tokens=-1), -2),                         # no persistent schedule
     (dict(head_dim=96), -3),
     (dict(block_size=8), -3),
     (dict(dtype=5), -3),
@@ -83,6 +84,15 @@ def test_append_rejects_bad_args(lib):
     assert f(ctypes.byref(_shape(head_dim=80)), FAKE, FAKE, FAKE, 1, FAKE, FAKE, None) == -3
     assert f(ctypes.byref(s), None, None, None, 0, None, None, None) == 0   # no tokens: no-op
     assert lib.pkv_launch_count() == 0
+
+
+def test_set_workspace_rejects_bad_args_before_device(lib):
+    f = lib.pkv_set_workspace
+    assert f(FAKE, 0) == -2                 # a workspace of no bytes
+    assert f(FAKE + 4, 4096) == -4          # not 16-byte aligned
+    # well-formed calls need the current device, which this host lacks
+    assert f(FAKE, 4096) == -6
+    assert f(None, 0) == -6
 
 
 def test_selftest_rejects_bad_limit_before_device(lib):
@@ -140,10 +150,94 @@ def test_binding_rejects_mismatched_extents(lib, monkeypatch, bad):
                       a["context_lens"], 0.125, out, max_context_len=16)
 
 
+class _NoDevice:
+    """Stands in for torch.cuda.device on a host without CUDA."""
+
+    def __init__(self, dev):
+        pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
 def test_binding_passes_consistent_extents_to_the_library(lib, monkeypatch):
+    import torch
     monkeypatch.setattr(B, "_dense", lambda *a, **k: None)
+    monkeypatch.setattr(B, "_one_device", lambda **t: torch.device("cuda", 0))
+    monkeypatch.setattr(B.torch.cuda, "device", _NoDevice)
     a = _decode_args()
     with pytest.raises(B.PkvError) as e:      # no GPU here: the library reports it
         B.paged_attn_decode(a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
                             a["context_lens"], 0.125, max_context_len=16)
     assert e.value.code == -6
+
+
+# ---------------------------------------------------------------- binding devices
+# Every tensor of a call must live on one GPU: the library launches on the
+# current device with that device's TMA descriptors, so another GPU's memory
+# must never reach it.  The rejection is host logic, checked here with
+# stand-ins for CUDA tensors and streams.
+class _FakeCuda:
+    def __init__(self, index):
+        import torch
+        self.is_cuda = True
+        self.device = torch.device("cuda", index)
+
+
+def test_one_device_rejects_mixed_and_host_tensors():
+    import torch
+    assert B._one_device(q=_FakeCuda(1), out=None, k_cache=_FakeCuda(1)) == torch.device("cuda", 1)
+    with pytest.raises(ValueError, match="k_cache is on cuda:1"):
+        B._one_device(q=_FakeCuda(0), k_cache=_FakeCuda(1))
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        B._one_device(q=_FakeCuda(0), block_tables=torch.zeros(2, dtype=torch.int32))
+
+
+def test_stream_of_another_device_is_rejected():
+    import torch
+
+    class S:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        B._stream_ptr(S(), torch.device("cuda", 0))
+
+
+def test_every_call_checks_all_its_tensors_for_one_device(lib, monkeypatch):
+    import torch
+    monkeypatch.setattr(B, "_dense", lambda *a, **k: None)
+    seen = {}
+
+    class Stop(Exception):
+        pass
+
+    def spy(**tensors):
+        seen.update(tensors)
+        raise Stop
+
+    monkeypatch.setattr(B, "_one_device", spy)
+    a = _decode_args()
+    out = torch.zeros_like(a["q"])
+    ws = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(Stop):
+        B.paged_attn_decode(a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
+                            a["context_lens"], 0.125, out, max_context_len=16, workspace=ws)
+    assert set(seen) == {"q", "k_cache", "v_cache", "block_tables", "context_lens", "out",
+                         "workspace"}
+    seen.clear()
+    k_new = torch.zeros(2, 2, 64, dtype=torch.float16)
+    with pytest.raises(Stop):
+        B.decode_step(a["q"], k_new, k_new.clone(), a["k_cache"], a["v_cache"],
+                      a["block_tables"], a["context_lens"], 0.125, out, max_context_len=16,
+                      workspace=ws)
+    assert set(seen) == {"q", "k_new", "v_new", "k_cache", "v_cache", "block_tables",
+                         "context_lens", "out", "workspace"}
+    seen.clear()
+    with pytest.raises(Stop):
+        B.kv_cache_append(k_new, k_new.clone(), torch.zeros(2, dtype=torch.int32),
+                          a["k_cache"][:, :, :, :], a["v_cache"])
+    assert set(seen) == {"k", "v", "slot_mapping", "k_cache", "v_cache"}

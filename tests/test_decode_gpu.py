@@ -33,38 +33,25 @@ def test_small_workloads(pkv, name, seed):
     assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), f"{name}/{seed}")
 
 
-def test_schedule_selection(pkv):
-    """split_tokens 0 picks partitions, -1 the persistent schedule; the
-    tensor-core variant serves group sizes of 3 and more."""
+def test_plan_selection(pkv):
+    """split_tokens 0 lets the library choose the partition size, > 0 forces
+    it; the tensor-core variant serves group sizes of 3 and more."""
     for name in W.ORDER:
         w = W.make(SMALL[name], seed=0)
         d = device_inputs(w)
-        for split, sched in ((0, 0), (-1, 1), (64, 0)):
+        for split in (0, 64):
             plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
                                                     w.max_context_len, split))
-            assert plan.schedule == sched
+            assert plan.schedule == 0
             assert plan.variant == (0 if w.spec.group <= 2 else 1)
         assert plan.split_tokens == 64
 
 
-@pytest.mark.parametrize("seed", [0, 1])
-@pytest.mark.parametrize("name", W.ORDER)
-def test_persistent_schedule_small_workloads(pkv, name, seed):
-    w = W.make(SMALL[name], seed=seed)
-    assert_close(widen_out(gpu_decode(pkv, w, split_tokens=-1)), oracle_decode(w),
-                 f"persistent {name}/{seed}")
-
-
-def test_large_batch_uses_partition_schedule(pkv):
-    """More than 2048 sequences fall back to the partition schedule even when
-    the persistent one is asked for."""
+def test_large_batch(pkv):
+    """More than 2048 sequences of short contexts."""
     spec = W.scaled(W.WORKLOADS["llama3_8b_gqa"], 2100, 40)
     w = W.make(spec, seed=9)
-    d = device_inputs(w)
-    plan = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
-                                            w.max_context_len, -1))
-    assert plan.schedule == 0
-    assert_close(widen_out(gpu_decode(pkv, w, d, split_tokens=-1)), oracle_decode(w), "B=2100")
+    assert_close(widen_out(gpu_decode(pkv, w)), oracle_decode(w), "B=2100")
 
 
 @pytest.mark.parametrize("split", [16, 64, 256, 512, 1 << 20])
@@ -86,20 +73,20 @@ def test_shape_sweep(pkv, dtype, G, D, bs):
     lens = np.array([1, bs - 1, bs, bs + 1, 3 * bs + 5], dtype=np.int32)
     spec = W.scaled(spec, 5, int(lens.max()))
     w = W.make(spec, seed=G * 1000 + D + bs, lens=lens)
-    for split in (0, bs, -1):       # auto partitions, one-block partitions, persistent
+    for split in (0, bs, 2 * bs):   # auto partitions, one- and two-block partitions
         assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), oracle_decode(w),
                      f"G={G} D={D} bs={bs} split={split}")
 
 
 def test_edge_lengths(pkv):
     """ctx = 1, multiples of the block size and one either side, long tails,
-    under both schedules."""
+    with automatic and forced partitions."""
     lens = np.array([1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025], dtype=np.int32)
     for base in ("llama7b_mha", "llama3_8b_gqa", "long_ctx_gqa"):
         spec = W.scaled(W.WORKLOADS[base], len(lens), int(lens.max()))
         w = W.make(spec, seed=11, lens=lens)
         ref = oracle_decode(w)
-        for split in (0, 512, -1):
+        for split in (0, 512, 80):
             assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), ref,
                          f"{base} split={split}")
 
@@ -114,7 +101,7 @@ def test_few_blocks_and_single_long_sequence(pkv, B):
         spec = W.scaled(W.WORKLOADS[base], B, int(lens.max()))
         w = W.make(spec, seed=B, lens=lens)
         ref = oracle_decode(w)
-        for split in (0, -1):
+        for split in (0, 48):
             assert_close(widen_out(gpu_decode(pkv, w, split_tokens=split)), ref,
                          f"{base} B={B} split={split}")
 
@@ -187,15 +174,15 @@ def _sample_rows(w: W.Workload, n: int, rng) -> np.ndarray:
 
 @pytest.mark.parametrize("name", W.ORDER)
 def test_full_size_sampled(pkv, name):
-    """Full-size workloads in the benchmark's launch configuration (and the
-    persistent schedule); the oracle recomputes a sample of (sequence, head)
-    rows one by one."""
+    """Full-size workloads in the benchmark's launch configuration (and with
+    1024-token partitions forced); the oracle recomputes a sample of
+    (sequence, head) rows one by one."""
     w = W.make(name, seed=0, device="cuda")
     d = device_inputs(w)
     rows = _sample_rows(w, 48, np.random.default_rng(0))
     ref = oracle.decode_rows(rows, W.bits(w.q), W.bits(w.k_cache), W.bits(w.v_cache),
                              w.block_tables, w.context_lens, w.scale, w.spec.dtype)
-    for split in (0, -1):
+    for split in (0, 1024):
         out = widen_out(gpu_decode(pkv, w, d, split_tokens=split))
         assert np.all(np.isfinite(out))
         assert_close(out[rows[:, 0], rows[:, 1]], ref, f"{name} split={split}")
@@ -206,7 +193,9 @@ def test_full_size_sampled(pkv, name):
 @pytest.mark.parametrize("bs", [16, 32])
 def test_tcgen05_kernel(pkv, dtype, G, bs):
     """The tcgen05/TMEM kernel (kernel=3) on ragged lengths spanning several
-    128-token groups and partitions."""
+    128-token groups and partitions, including forced partitions that are not
+    a multiple of 128 tokens (80 and 208: every partition ends in a ragged
+    group)."""
     Hkv = 2
     spec = W.WorkloadSpec("tc", 6, G * Hkv, Hkv, 128, bs, dtype, 0, 0, "uniform", (1, 1))
     lens = np.array([1, 127, 128, 129, 700, 1500], dtype=np.int32)
@@ -217,7 +206,11 @@ def test_tcgen05_kernel(pkv, dtype, G, bs):
                                             w.max_context_len, 0, 3))
     assert plan.variant == 2 and plan.schedule == 0
     ref = oracle_decode(w)
-    for split in (0, 256, 1 << 20):
+    for split in (0, 256, 1 << 20, 80, 208):
+        if split in (80, 208):
+            sp = pkv.decode_plan(pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"],
+                                                  w.max_context_len, split, 3))
+            assert sp.split_tokens == -(-split // bs) * bs     # rounded to the block size only
         out = pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                                     d["context_lens"], w.scale, max_context_len=w.max_context_len,
                                     split_tokens=split, kernel=3)
@@ -236,7 +229,7 @@ def test_kernel_choice_rules(pkv):
     with pytest.raises(pkv.PkvError):
         pkv.decode_plan(shp(1))                          # CUDA cores need group <= 2
     with pytest.raises(pkv.PkvError):
-        pkv.decode_plan(shp(3, -1))                      # tcgen05 has no persistent schedule
+        pkv.decode_plan(shp(3, -1))                      # negative partition sizes
 
 
 @pytest.mark.parametrize("kernel", [0, 3])

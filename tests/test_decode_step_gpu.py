@@ -78,9 +78,10 @@ def test_fused_step_full_continuous_batching(pkv):
 
 
 @pytest.mark.parametrize("name", W.ORDER)
-def test_fused_step_persistent_schedule(pkv, name):
-    """The persistent stream-K schedule with the append fused: equal to append
-    + decode on that schedule bit for bit, caches included, and to the
+def test_fused_step_forced_partitions(pkv, name):
+    """The append fused under short forced partitions (48 tokens, so the new
+    token lands in the first, a middle or the last partition of a sequence):
+    equal to append + decode bit for bit, caches included, and to the
     oracle."""
     w = W.make(SMALL[name], seed=7)
     d = device_inputs(w)
@@ -88,15 +89,15 @@ def test_fused_step_persistent_schedule(pkv, name):
     pkv.kv_cache_append(w.k_new.cuda(), w.v_new.cuda(), torch.from_numpy(w.slot_mapping).cuda(),
                         kc2, vc2)
     o2 = pkv.paged_attn_decode(d["q"], kc2, vc2, d["block_tables"], d["context_lens"], w.scale,
-                               max_context_len=w.max_context_len, split_tokens=-1)
-    of, kf, vf = _fused(pkv, w, d, split_tokens=-1)
+                               max_context_len=w.max_context_len, split_tokens=48)
+    of, kf, vf = _fused(pkv, w, d, split_tokens=48)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
     assert _same(kf, kc2) and _same(vf, vc2) and _same(of, o2)
     ek, ev = oracle.append(W.bits(w.k_new), W.bits(w.v_new), w.slot_mapping,
                            W.bits(w.k_cache), W.bits(w.v_cache))
     assert np.array_equal(W.bits(kf), ek) and np.array_equal(W.bits(vf), ev)
-    assert_close(widen_out(of), oracle_decode(w, ek, ev), f"persistent fused {name}")
+    assert_close(widen_out(of), oracle_decode(w, ek, ev), f"forced-partition fused {name}")
 
 
 @pytest.mark.parametrize("G", [4, 8, 32])

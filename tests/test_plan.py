@@ -128,7 +128,7 @@ def test_benchmark_workload_plans(lib):
         assert p.workspace_bytes == rows * (spec.head_dim * 4 + 8), name
 
 
-def test_tcgen05_and_persistent_plans(lib):
+def test_tcgen05_plans(lib):
     # tcgen05 kernel: 2048-token partitions (4096 for more than 16 heads), 128-token grain
     p = plan_for(lib, GB300_SMS, num_seqs=128, num_q_heads=32, num_kv_heads=8,
                  max_context_len=8192, dtype=B.PKV_BF16, kernel=3)
@@ -139,24 +139,19 @@ def test_tcgen05_and_persistent_plans(lib):
     p = plan_for(lib, GB300_SMS, num_seqs=2, num_q_heads=8, num_kv_heads=2,
                  max_context_len=1000, kernel=3)
     assert p.variant == 2 and p.split_tokens % 128 == 0
-    # persistent schedule: 2 resident CTAs per SM plus 4 per SM dispatched later
-    p = plan_for(lib, 100, num_seqs=64, num_q_heads=32, num_kv_heads=32,
-                 max_context_len=4096, split_tokens=-1)
-    assert (p.schedule, p.split_tokens, p.num_splits, p.grid_ctas) == (1, 0, 0, 600)
-    hdr = -(-((9 + 64) * 4) // 256) * 256
-    W_ = 600 * p.warps_per_cta
-    assert p.workspace_bytes == hdr + 2 * W_ * 1 * 8 + 2 * W_ * 1 * 128 * 4
-    # more than 2048 sequences fall back to partitions
-    p = plan_for(lib, 100, num_seqs=4096, num_q_heads=8, num_kv_heads=8,
-                 max_context_len=64, split_tokens=-1)
-    assert p.schedule == 0
+    # a forced partition is rounded to the block size only (the kernel walks
+    # it in 128-token groups, the last one ragged)
+    for forced, want in ((80, 80), (208, 208), (70, 80)):
+        p = plan_for(lib, GB300_SMS, num_seqs=2, num_q_heads=8, num_kv_heads=2,
+                     max_context_len=1000, split_tokens=forced, kernel=3)
+        assert (p.variant, p.split_tokens, p.num_splits) == (2, want, -(-1000 // want))
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(num_q_heads=64, num_kv_heads=1), ERR_UNSUPPORTED),   # group of 64
     (dict(num_q_heads=8, num_kv_heads=2, kernel=1), ERR_UNSUPPORTED),  # CUDA cores, group 4
     (dict(head_dim=64, kernel=3), ERR_UNSUPPORTED),            # tcgen05 needs head_dim 128
-    (dict(kernel=3, split_tokens=-1), ERR_UNSUPPORTED),        # tcgen05 is partitions only
+    (dict(split_tokens=-1), ERR_INVALID),                       # no persistent schedule
     (dict(max_context_len=100, max_blocks_per_seq=4), ERR_INVALID),  # > MB * bs
 ])
 def test_rejected_shapes(lib, kw, code):

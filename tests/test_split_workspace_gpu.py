@@ -120,3 +120,48 @@ def test_bad_block_in_one_partition(pkv, spec, split, kernel):
     out = _decode(pkv, w, d, ws, split, kernel=kernel)
     assert pkv.get_device_error() == 0
     assert_close(widen_out(out), ref, "after the bad call")
+
+
+def test_set_workspace_serves_calls_without_one(pkv):
+    """pkv_set_workspace: a decode (and a fused step) given a NULL workspace
+    uses the one set for the device; one too small is reported before any
+    launch; host memory is refused; clearing it restores the error."""
+    import ctypes
+    lib = pkv.load_library()
+    w = W.make(LONG, seed=6)
+    d = device_inputs(w)
+    shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len)
+    need = pkv.decode_plan(shape).workspace_bytes
+    assert need > 0
+    ref = _oracle(w)
+    big = torch.empty(need + 4096, dtype=torch.uint8, device="cuda")
+    _fill(big, "ones")
+    args = (ctypes.byref(shape), d["q"].data_ptr(), d["k_cache"].data_ptr(),
+            d["v_cache"].data_ptr(), d["block_tables"].data_ptr(), d["context_lens"].data_ptr(),
+            ctypes.c_float(w.scale))
+    stream = torch.cuda.current_stream().cuda_stream
+    try:
+        assert lib.pkv_set_workspace(big.data_ptr(), need + 4096) == 0
+        out = torch.full_like(d["q"], float("nan"))
+        assert lib.pkv_paged_attn_decode(*args, out.data_ptr(), None, 0, stream) == 0
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert_close(widen_out(out), ref, "set workspace, C ABI")
+        # the binding passes no workspace once one is set for the device
+        pkv.set_workspace(big)
+        n0 = pkv.launch_count()
+        out2 = _decode(pkv, w, d, None, 0)
+        assert pkv.launch_count() - n0 == 2
+        assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+        # too small: rejected on the host, nothing launched
+        small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+        assert lib.pkv_set_workspace(small.data_ptr(), need - 16) == 0
+        n0 = pkv.launch_count()
+        assert lib.pkv_paged_attn_decode(*args, out.data_ptr(), None, 0, stream) == -5
+        assert pkv.launch_count() == n0
+        # host memory is not a device workspace
+        host = torch.empty(need, dtype=torch.uint8).pin_memory()
+        assert lib.pkv_set_workspace(host.data_ptr(), need) == -2
+    finally:
+        pkv.set_workspace(None)
+    assert lib.pkv_paged_attn_decode(*args, out.data_ptr(), None, 0, stream) == -5
