@@ -111,7 +111,7 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, cudaStream_t
                              Args... args) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kReduceThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -122,22 +122,31 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Reduce grid: CTAs of kReduceThreads threads, each over a contiguous range
+// of at most kReduceMaxRows rows; at most two per SM unless the rows need more.
 template <bool BF>
-cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>((a.B * a.Hq + 7) / 8);
+cudaError_t launch_reduce(const DecodeArgs& a, int D, int sms, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.B) * a.Hq;
+  const int warps = kReduceThreads / 32;
+  long long grid = (rows + warps - 1) / warps;
+  if (grid > 2ll * sms) grid = 2ll * sms;
+  const long long need = (rows + kReduceMaxRows - 1) / kReduceMaxRows;
+  if (grid < need) grid = need;
+  const int per = static_cast<int>((rows + grid - 1) / grid);
   const float* po = a.part_o;
   const float2* pml = a.part_ml;
   const int32_t* cl = a.context_lens;
+  const unsigned g = static_cast<unsigned>(grid);
   switch (D) {
     case 64:
-      return launch_dependent(split_reduce_kernel<BF, 64>, grid, stream, po, pml, cl, a.out, a.B,
-                              a.Hq, a.S, a.P, a.max_ctx);
+      return launch_dependent(split_reduce_kernel<BF, 64>, g, stream, po, pml, cl, a.out, a.B,
+                              a.Hq, a.S, a.P, a.max_ctx, per);
     case 128:
-      return launch_dependent(split_reduce_kernel<BF, 128>, grid, stream, po, pml, cl, a.out, a.B,
-                              a.Hq, a.S, a.P, a.max_ctx);
+      return launch_dependent(split_reduce_kernel<BF, 128>, g, stream, po, pml, cl, a.out, a.B,
+                              a.Hq, a.S, a.P, a.max_ctx, per);
     case 256:
-      return launch_dependent(split_reduce_kernel<BF, 256>, grid, stream, po, pml, cl, a.out, a.B,
-                              a.Hq, a.S, a.P, a.max_ctx);
+      return launch_dependent(split_reduce_kernel<BF, 256>, g, stream, po, pml, cl, a.out, a.B,
+                              a.Hq, a.S, a.P, a.max_ctx, per);
     default:
       return cudaErrorInvalidValue;
   }
@@ -558,7 +567,7 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   g_launches.fetch_add(1);
   if (plan.num_splits > 1) {
-    e = bf ? launch_reduce<true>(a, D, st) : launch_reduce<false>(a, D, st);
+    e = bf ? launch_reduce<true>(a, D, d->sms, st) : launch_reduce<false>(a, D, d->sms, st);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     g_launches.fetch_add(1);
   }

@@ -109,25 +109,23 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   // after that
   pdl_wait();
   pdl_launch_dependents();
+  // block ids and length in one round trip, as in paged_decode_kernel
+  const int t0 = split * a.P;
+  const int j0 = t0 / BS;
+  PartitionIds<LY::THREADS> pid;
+  pid.load(a.block_tables + (size_t)seq * a.MB + j0, min(a.P / BS, a.MB - j0));
   const int L = a.context_lens[seq];
   if (L < 1 || L > a.max_ctx) {
     if (tid == 0 && split == 0 && kvh == 0) record_error(a.err, kDevBadContext);
     return;
   }
-  const int t0 = split * a.P;
   if (t0 >= L) return;
   const int t1 = min(t0 + a.P, L);
-  const int j0 = t0 / BS;
   const int nblk = (t1 - t0 + BS - 1) / BS;
   const int ngroups = (t1 - t0 + 127) / 128;
   const size_t row0 = (size_t)seq * a.Hq + (size_t)kvh * a.G;
 
-  bool bad = false;
-  for (int k = tid; k < nblk; k += LY::THREADS) {
-    const int p = __ldg(a.block_tables + (size_t)seq * a.MB + j0 + k);
-    bad |= (p < 0) | (p >= a.NB);
-    ids[k] = p;
-  }
+  const bool bad = pid.store(ids, nblk, a.NB);
   if (tid < LY::NBAR) {
     const bool many = (tid >= LY::B_SFREE && tid < LY::B_SFREE + 2) ||
                       (tid >= LY::B_PFULL && tid < LY::B_PFULL + LY::PBUF);
