@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(256)
 template <class... KArgs, class... Args>
 cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, cudaStream_t stream,
                              Args... args) {
+  static_assert(sizeof...(KArgs) == sizeof...(Args), "argument count");
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kReduceThreads);
@@ -122,33 +123,31 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// Reduce grid: CTAs of kReduceThreads threads, each over a contiguous range
-// of at most kReduceMaxRows rows; at most two per SM unless the rows need more.
-template <bool BF>
-cudaError_t launch_reduce(const DecodeArgs& a, int D, int sms, cudaStream_t stream) {
+// Reduce grid: one warp per (sequence, query head) row.  The smallest
+// variant that loads every partial of a row in one batch: two splits (the
+// 40-register build, so that the most warps are resident), up to the 64-
+// register build's batch, else the 128-register build.
+template <bool BF, int D>
+cudaError_t launch_reduce_d(const DecodeArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.B) * a.Hq;
   const int warps = kReduceThreads / 32;
-  long long grid = (rows + warps - 1) / warps;
-  if (grid > 2ll * sms) grid = 2ll * sms;
-  const long long need = (rows + kReduceMaxRows - 1) / kReduceMaxRows;
-  if (grid < need) grid = need;
-  const int per = static_cast<int>((rows + grid - 1) / grid);
-  const float* po = a.part_o;
-  const float2* pml = a.part_ml;
-  const int32_t* cl = a.context_lens;
-  const unsigned g = static_cast<unsigned>(grid);
+  const unsigned g = static_cast<unsigned>((rows + warps - 1) / warps);
+  auto kern = a.S <= reduce_batch(D, 1) ? split_reduce_kernel<BF, D, 1>
+                                         : split_reduce_kernel<BF, D, 2>;
+  if constexpr (D <= 128) {   // at head_dim 256 the 40-register build would spill
+    if (a.S <= reduce_batch(D, 0)) kern = split_reduce_kernel<BF, D, 0>;
+  }
+  return launch_dependent(kern, g, stream, a.part_o, a.part_ml, a.context_lens, a.out, a.B, a.Hq,
+                          a.S, a.P, a.max_ctx);
+}
+
+template <bool BF>
+cudaError_t launch_reduce(const DecodeArgs& a, int D, cudaStream_t stream) {
   switch (D) {
-    case 64:
-      return launch_dependent(split_reduce_kernel<BF, 64>, g, stream, po, pml, cl, a.out, a.B,
-                              a.Hq, a.S, a.P, a.max_ctx, per);
-    case 128:
-      return launch_dependent(split_reduce_kernel<BF, 128>, g, stream, po, pml, cl, a.out, a.B,
-                              a.Hq, a.S, a.P, a.max_ctx, per);
-    case 256:
-      return launch_dependent(split_reduce_kernel<BF, 256>, g, stream, po, pml, cl, a.out, a.B,
-                              a.Hq, a.S, a.P, a.max_ctx, per);
-    default:
-      return cudaErrorInvalidValue;
+    case 64: return launch_reduce_d<BF, 64>(a, stream);
+    case 128: return launch_reduce_d<BF, 128>(a, stream);
+    case 256: return launch_reduce_d<BF, 256>(a, stream);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -567,7 +566,7 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   g_launches.fetch_add(1);
   if (plan.num_splits > 1) {
-    e = bf ? launch_reduce<true>(a, D, d->sms, st) : launch_reduce<false>(a, D, d->sms, st);
+    e = bf ? launch_reduce<true>(a, D, st) : launch_reduce<false>(a, D, st);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     g_launches.fetch_add(1);
   }

@@ -381,41 +381,6 @@ struct MmaCompute {
   }
 };
 
-// ------------------------------------------------------------------ gather
-// Block-table entries of one partition (indirect addressing), loaded before
-// the context length is known so that the two loads share one round trip:
-// thread t holds entries t, t + NT, ... of the partition's part of the table
-// row.  Entries past the sequence's last block are loaded but never used or
-// range-checked.
-template <int NT>
-struct PartitionIds {
-  static constexpr int R = (kMaxBlocksPerCta + NT - 1) / NT;
-  int v[R];
-
-  // row: the partition's first entry; n: entries of the partition inside the row
-  __device__ __forceinline__ void load(const int32_t* row, int n) {
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int k = static_cast<int>(threadIdx.x) + r * NT;
-      v[r] = k < n ? __ldg(row + k) : -1;
-    }
-  }
-
-  // Copies the first nblk entries to ids; true if one is outside [0, NB).
-  __device__ __forceinline__ bool store(int* ids, int nblk, int NB) const {
-    bool bad = false;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int k = static_cast<int>(threadIdx.x) + r * NT;
-      if (k < nblk) {
-        bad |= (v[r] < 0) | (v[r] >= NB);
-        ids[k] = v[r];
-      }
-    }
-    return bad;
-  }
-};
-
 // ------------------------------------------------------------------ kernel
 template <bool BF, int D, int BS, int NW, int NS, class Compute>
 __global__ void __launch_bounds__(NW * 32, 1)
@@ -457,13 +422,18 @@ __global__ void __launch_bounds__(NW * 32, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  // The partition's block ids and the context length, in one round trip
-  // (split < S keeps j0 inside the row: t0 < max_context_len <= MB * bs).
+  // Block-table gather for this partition (indirect addressing), range-
+  // checked.  The first partition of a sequence is never empty, so it loads
+  // its block ids while the context length is in flight (one round trip for
+  // both); the others load them once the length shows they are not empty (an
+  // empty CTA then exits after a single load).  split < S keeps j0 inside the
+  // row: t0 < max_context_len <= MB * bs.
   const int t0 = split * a.P;
   const int j0 = t0 / BS;
-  PartitionIds<NW * 32> pid;
-  pid.load(a.block_tables + (size_t)seq * a.MB + j0, min(a.P / BS, a.MB - j0));
+  const int32_t* trow = a.block_tables + (size_t)seq * a.MB + j0;
   const int L = a.context_lens[seq];
+  if (split == 0)
+    for (int k = threadIdx.x; k < min(a.P / BS, a.MB - j0); k += NW * 32) ids[k] = __ldg(trow + k);
   if (L < 1 || L > a.max_ctx) {
     if (threadIdx.x == 0 && split == 0 && kvh == 0) record_error(a.err, kDevBadContext);
     return;
@@ -471,9 +441,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
   if (t0 >= L) return;
   const int t1 = min(t0 + a.P, L);
   const int nblk = (t1 - t0 + BS - 1) / BS;
-
-  // Block-table gather for this partition (indirect addressing), range-checked.
-  const bool bad = pid.store(ids, nblk, a.NB);
+  bool bad = false;
+  for (int k = threadIdx.x; k < nblk; k += NW * 32) {
+    const int p = split == 0 ? ids[k] : __ldg(trow + k);   // ids[k]: this thread's own store
+    bad |= (p < 0) | (p >= a.NB);
+    ids[k] = p;
+  }
   if (threadIdx.x < NW * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
   if (threadIdx.x == 0) fence_mbar_init();
   if (__syncthreads_or(bad)) {
@@ -587,119 +560,113 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 // ------------------------------------------------------------------ reduce
-// Rows of one reduce CTA at most (a shared-memory list of its merging rows).
-constexpr int kReduceMaxRows = 256;
-constexpr int kReduceThreads = 512;
+constexpr int kReduceThreads = 128;   // four warps: one (sequence, query head) row each
 
-// Cross-split reduce: every (sequence, query head) row with more than one
-// split.  M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
-// summed in split order (deterministic).  A few CTAs of 16 warps (two per SM
-// at most, launched while the decode grid drains, so that they are resident
-// when it completes) each own a contiguous range of rows: before the
-// dependency wait they list the rows whose length spans more than one
-// partition (the lengths were written before the decode grid started), and
-// after it each warp merges listed rows.  In a row, lane j holds (m, l) of
-// split j (of each group of 32 splits) and hands w_j to the others by
-// shuffle; each lane owns D / 32 output elements and keeps the loads of up to
-// J partials in flight (the first batch together with the (m, l) loads).
-template <bool BF, int D>
-__global__ void __launch_bounds__(kReduceThreads, 2)
+// Partials a reduce lane keeps in flight, by variant: 0 (two splits; at most
+// 40 registers, so that twelve CTAs fit an idle SM) two partials; 1 (at
+// most 64 registers: a CTA fits on an SM next to three decode CTAs, eight on
+// an idle one) 32 floats; 2 (many splits) 64 floats.
+constexpr int reduce_batch(int D, int variant) {
+  return variant == 0 ? 2 : ((variant == 2 ? 64 : 32) / (D / 32) > 32 ? 32 : (variant == 2 ? 64 : 32) / (D / 32));
+}
+// Registers per thread the variant is built for.
+constexpr int reduce_regs(int variant) { return variant == 0 ? 40 : (variant == 1 ? 64 : 128); }
+
+// Cross-split reduce: one warp per (sequence, query head) row with more than
+// one split.  M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s
+// w_s l_s, summed in split order (deterministic).  The CTAs are small, so
+// that many are resident while the decode grid drains and when it completes.
+// Lane j holds (m, l) of split j (of each group of 32 splits) and hands w_j
+// to the other lanes by shuffle; each lane owns D / 32 output elements and
+// keeps the loads of up to J partials in flight (the first batch together
+// with the (m, l) loads); three builds differ only in J and their register
+// budget.
+template <bool BF, int D, int V>
+__global__ void __launch_bounds__(kReduceThreads, 65536 / (kReduceThreads * reduce_regs(V)))
     split_reduce_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                         const int32_t* __restrict__ context_lens, uint16_t* __restrict__ out,
-                        int B, int Hq, int S, int P, int max_ctx, int rows_per_cta) {
+                        int B, int Hq, int S, int P, int max_ctx) {
   constexpr int OPL = D / 32;               // output elements per lane: 2, 4 or 8
-  constexpr int J = OPL >= 8 ? 4 : 8;       // partials loaded per batch
-  __shared__ int list_row[kReduceMaxRows];
-  __shared__ int list_n[kReduceMaxRows];
-  __shared__ int count;
+  constexpr int J = reduce_batch(D, V);     // partials loaded per batch
   // the next kernel on the stream may become resident meanwhile
   pdl_launch_dependents();
-  const int rows = B * Hq;
-  const int r0 = blockIdx.x * rows_per_cta;
-  const int nr = min(rows_per_cta, rows - r0);
-  if (threadIdx.x == 0) count = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < nr; i += kReduceThreads) {
-    const int L = context_lens[(r0 + i) / Hq];
-    if (L > P && L <= max_ctx) {   // more than one partition (and a valid length)
-      const int k = atomicAdd(&count, 1);
-      list_row[k] = r0 + i;
-      list_n[k] = (L + P - 1) / P;
-    }
-  }
-  __syncthreads();
-  // the partials only after the decode grid has completed
-  pdl_wait();
+  const int gw = blockIdx.x * (kReduceThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  for (int k = threadIdx.x >> 5; k < count; k += kReduceThreads / 32) {
-    const int gw = list_row[k], n = list_n[k];
-    const float2* ml = part_ml + (size_t)gw * S;
-    const float* po = part_o + (size_t)gw * S * D + lane * OPL;
-    // partials s_begin .. s_begin + cnt - 1 (cnt <= J) into x
-    auto load = [&](float (&x)[J][OPL], int s_begin, int cnt) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        if (j < cnt) {
-          const float* src = po + (size_t)(s_begin + j) * D;
-#pragma unroll
-          for (int e = 0; e < OPL; e += 2) {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src + e));
-            x[j][e] = t.x;
-            x[j][e + 1] = t.y;
-          }
-        }
-      }
-    };
-    // acc += w_s x_s for the splits j0 .. of the current group of 32, w_s held by lane s % 32
-    float acc[OPL];
-#pragma unroll
-    for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
-    auto accumulate = [&](const float (&x)[J][OPL], float w, int j0, int cnt) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const float wj = __shfl_sync(kFull, w, (j0 + j) & 31);
-        if (j0 + j < cnt) {
-#pragma unroll
-          for (int e = 0; e < OPL; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
-        }
-      }
-    };
-
-    // The first batch of partials is in flight together with the (m, l) loads.
-    float x[J][OPL];
-    const int cnt0 = min(32, n);
-    load(x, 0, min(J, cnt0));
-    const float2 first = lane < n ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
-    float M = first.x;
-    for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-
-    float lsum = 0.f;
-    float w = lane < n ? fast_exp2(first.x - M) : 0.f;
-    if (lane < n) lsum = fmaf(w, first.y, lsum);
-    accumulate(x, w, 0, cnt0);
-    for (int j0 = J; j0 < cnt0; j0 += J) {
-      load(x, j0, min(J, cnt0 - j0));
-      accumulate(x, w, j0, cnt0);
-    }
-    for (int s0 = 32; s0 < n; s0 += 32) {
-      const bool mine = s0 + lane < n;
-      const float2 v = mine ? __ldcg(ml + s0 + lane) : make_float2(0.f, 0.f);
-      w = mine ? fast_exp2(v.x - M) : 0.f;
-      if (mine) lsum = fmaf(w, v.y, lsum);
-      const int cnt = min(32, n - s0);
-      for (int j0 = 0; j0 < cnt; j0 += J) {
-        load(x, s0 + j0, min(J, cnt - j0));
-        accumulate(x, w, j0, cnt);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
-    uint16_t* orow = out + (size_t)gw * D + lane * OPL;
-#pragma unroll
-    for (int e = 0; e < OPL; ++e) orow[e] = to_elem<BF>(acc[e] / lsum);
+  // The lengths were written before the decode grid started, so they can be
+  // read before waiting for it; the partials only after.
+  int n = 0;
+  if (gw < B * Hq) {
+    const int L = context_lens[gw / Hq];
+    if (L >= 1 && L <= max_ctx) n = (L + P - 1) / P;
   }
+  pdl_wait();
+  if (n <= 1) return;
+  const float2* ml = part_ml + (size_t)gw * S;
+  const float* po = part_o + (size_t)gw * S * D + lane * OPL;
+  // partials s_begin .. s_begin + cnt - 1 (cnt <= J) into x
+  auto load = [&](float (&x)[J][OPL], int s_begin, int cnt) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      if (j < cnt) {
+        const float* src = po + (size_t)(s_begin + j) * D;
+#pragma unroll
+        for (int e = 0; e < OPL; e += 2) {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src + e));
+          x[j][e] = t.x;
+          x[j][e + 1] = t.y;
+        }
+      }
+    }
+  };
+  // acc += w_s x_s for the splits j0 .. of the current group of 32, w_s held by lane s % 32
+  float acc[OPL];
+#pragma unroll
+  for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
+  auto accumulate = [&](const float (&x)[J][OPL], float w, int j0, int cnt) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float wj = __shfl_sync(kFull, w, (j0 + j) & 31);
+      if (j0 + j < cnt) {
+#pragma unroll
+        for (int e = 0; e < OPL; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
+      }
+    }
+  };
+
+  // The first batch of partials is in flight together with the (m, l) loads.
+  float x[J][OPL];
+  const int cnt0 = min(32, n);
+  load(x, 0, min(J, cnt0));
+  const float2 first = lane < n ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+  float M = first.x;
+  for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+
+  float lsum = 0.f;
+  float w = lane < n ? fast_exp2(first.x - M) : 0.f;
+  if (lane < n) lsum = fmaf(w, first.y, lsum);
+  accumulate(x, w, 0, cnt0);
+  for (int j0 = J; j0 < cnt0; j0 += J) {
+    load(x, j0, min(J, cnt0 - j0));
+    accumulate(x, w, j0, cnt0);
+  }
+  for (int s0 = 32; s0 < n; s0 += 32) {
+    const bool mine = s0 + lane < n;
+    const float2 v = mine ? __ldcg(ml + s0 + lane) : make_float2(0.f, 0.f);
+    w = mine ? fast_exp2(v.x - M) : 0.f;
+    if (mine) lsum = fmaf(w, v.y, lsum);
+    const int cnt = min(32, n - s0);
+    for (int j0 = 0; j0 < cnt; j0 += J) {
+      load(x, s0 + j0, min(J, cnt - j0));
+      accumulate(x, w, j0, cnt);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+  uint16_t* orow = out + (size_t)gw * D + lane * OPL;
+#pragma unroll
+  for (int e = 0; e < OPL; ++e) orow[e] = to_elem<BF>(acc[e] / lsum);
 }
 
 }  // namespace pkv

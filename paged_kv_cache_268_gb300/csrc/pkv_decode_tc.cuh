@@ -109,12 +109,13 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   // after that
   pdl_wait();
   pdl_launch_dependents();
-  // block ids and length in one round trip, as in paged_decode_kernel
+  // block ids and length, as in paged_decode_kernel
   const int t0 = split * a.P;
   const int j0 = t0 / BS;
-  PartitionIds<LY::THREADS> pid;
-  pid.load(a.block_tables + (size_t)seq * a.MB + j0, min(a.P / BS, a.MB - j0));
+  const int32_t* trow = a.block_tables + (size_t)seq * a.MB + j0;
   const int L = a.context_lens[seq];
+  if (split == 0)
+    for (int k = tid; k < min(a.P / BS, a.MB - j0); k += LY::THREADS) ids[k] = __ldg(trow + k);
   if (L < 1 || L > a.max_ctx) {
     if (tid == 0 && split == 0 && kvh == 0) record_error(a.err, kDevBadContext);
     return;
@@ -125,7 +126,12 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   const int ngroups = (t1 - t0 + 127) / 128;
   const size_t row0 = (size_t)seq * a.Hq + (size_t)kvh * a.G;
 
-  const bool bad = pid.store(ids, nblk, a.NB);
+  bool bad = false;
+  for (int k = tid; k < nblk; k += LY::THREADS) {
+    const int p = split == 0 ? ids[k] : __ldg(trow + k);
+    bad |= (p < 0) | (p >= a.NB);
+    ids[k] = p;
+  }
   if (tid < LY::NBAR) {
     const bool many = (tid >= LY::B_SFREE && tid < LY::B_SFREE + 2) ||
                       (tid >= LY::B_PFULL && tid < LY::B_PFULL + LY::PBUF);

@@ -123,3 +123,35 @@ def test_fused_step_tcgen05(pkv, G, bs):
                            W.bits(w.k_cache), W.bits(w.v_cache))
     assert np.array_equal(W.bits(kf), ek) and np.array_equal(W.bits(vf), ev)
     assert_close(widen_out(of), oracle_decode(w, ek, ev), f"tcgen05 fused G={G} bs={bs}")
+
+
+@pytest.mark.parametrize("G", [12, 32])
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 32), (128, 32)])
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+def test_fused_step_wide_groups(pkv, G, D, bs, dtype):
+    """Wide query groups on mma.sync (warp pairs where the stages are 8 KB or
+    less: the first warp of a pair writes the new row into the staged tile,
+    the second waits for it): caches and output equal append + decode bit for
+    bit, with automatic and short forced partitions, and match the oracle.
+    Lengths put the new token at the start, middle and end of a block."""
+    lens = np.array([1, bs, bs + 1, 2 * bs - 1, 300, 777, 1500], dtype=np.int32)
+    spec = W.WorkloadSpec("widestep", len(lens), G * 2, 2, D, bs, dtype, 0, 0, "uniform", (1, 1))
+    spec = W.scaled(spec, len(lens), int(lens.max()))
+    w = W.make(spec, seed=5 * G + D + bs, lens=lens)
+    d = device_inputs(w)
+    ek, ev = oracle.append(W.bits(w.k_new), W.bits(w.v_new), w.slot_mapping,
+                           W.bits(w.k_cache), W.bits(w.v_cache))
+    ref = oracle_decode(w, ek, ev)
+    for split in (0, 3 * bs):
+        kc2, vc2 = d["k_cache"].clone(), d["v_cache"].clone()
+        pkv.kv_cache_append(w.k_new.cuda(), w.v_new.cuda(),
+                            torch.from_numpy(w.slot_mapping).cuda(), kc2, vc2)
+        o2 = pkv.paged_attn_decode(d["q"], kc2, vc2, d["block_tables"], d["context_lens"],
+                                   w.scale, max_context_len=w.max_context_len,
+                                   split_tokens=split)
+        of, kf, vf = _fused(pkv, w, d, split_tokens=split)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert _same(kf, kc2) and _same(vf, vc2) and _same(of, o2), f"G={G} D={D} split={split}"
+        assert np.array_equal(W.bits(kf), ek) and np.array_equal(W.bits(vf), ev)
+        assert_close(widen_out(of), ref, f"wide fused G={G} D={D} bs={bs} split={split}")
