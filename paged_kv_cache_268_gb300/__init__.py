@@ -18,5 +18,7 @@ from ._binding import (  # noqa: F401
     launch_count,
     load_library,
     paged_attn_decode,
+    selftest_wait_timeout,
+    set_workspace,
     workspace_bytes,
 )
