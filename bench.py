@@ -792,7 +792,7 @@ def run_pkv(args):
                    "sum_context_len": int(w.context_lens.sum()), "seed": args.seed,
                    "step": ("kv_cache_append(1 token/seq) + paged_attn_decode" if args.two_call
                             else "decode_step: append of 1 token/seq fused into paged decode"),
-                   "schedule": "persistent" if plan.schedule == 1 else "partitions",
+                   "schedule": "partitions",
                    "grid_ctas": plan.grid_ctas,
                    "split_tokens": plan.split_tokens, "num_splits": plan.num_splits,
                    "kernel_variant": ["cuda-core", "mma.sync", "tcgen05"][plan.variant],

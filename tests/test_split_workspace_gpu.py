@@ -165,3 +165,54 @@ def test_set_workspace_serves_calls_without_one(pkv):
     finally:
         pkv.set_workspace(None)
     assert lib.pkv_paged_attn_decode(*args, out.data_ptr(), None, 0, stream) == -5
+
+
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 16), (256, 32)])
+def test_reduce_builds_at_their_split_counts(pkv, D, bs):
+    """The split reduce has three builds, chosen by the split count: two
+    splits (the 40-register build; head_dim 256 uses the next one), up to
+    the 64-register build's batch, and more.  Forced partition sizes put the
+    longest sequence at each boundary; every row must match the oracle."""
+    lens = np.array([1, bs, 2 * bs + 3, 300, 1200, 2000], dtype=np.int32)
+    spec = W.WorkloadSpec("reduce", len(lens), 8, 2, D, bs, W.BF16, 0, 0, "uniform", (1, 1))
+    spec = W.scaled(spec, len(lens), int(lens.max()))
+    w = W.make(spec, seed=D + bs, lens=lens)
+    d = device_inputs(w)
+    ref = _oracle(w)
+    Lmax = int(lens.max())
+    for S in (2, 3, 8, 9, 16, 17, 33):
+        split = -(-(-(-Lmax // S)) // bs) * bs          # partition size giving about S splits
+        shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len, split)
+        plan = pkv.decode_plan(shape)
+        ws = torch.empty(max(plan.workspace_bytes, 16), dtype=torch.uint8, device="cuda")
+        _fill(ws, "ones")
+        out = _decode(pkv, w, d, ws, split)
+        assert pkv.get_device_error() == 0
+        assert_close(widen_out(out), ref, f"D={D} bs={bs} S={plan.num_splits}")
+
+
+def test_set_workspace_serves_the_fused_step(pkv):
+    """pkv_decode_step with a NULL workspace uses the set one, like the plain
+    decode: same output and caches as with an explicit workspace."""
+    w = W.make(GQA, seed=8)
+    d = device_inputs(w)
+    shape = pkv.decode_shape(d["q"], d["k_cache"], d["block_tables"], w.max_context_len)
+    assert pkv.decode_plan(shape).workspace_bytes > 0
+    k_new, v_new = w.k_new.cuda(), w.v_new.cuda()
+    kc1, vc1 = d["k_cache"].clone(), d["v_cache"].clone()
+    ref = pkv.decode_step(d["q"], k_new, v_new, kc1, vc1, d["block_tables"], d["context_lens"],
+                          w.scale, max_context_len=w.max_context_len,
+                          workspace=pkv.alloc_workspace(shape))
+    big = pkv.alloc_workspace(shape)
+    _fill(big, "random", 3)
+    kc2, vc2 = d["k_cache"].clone(), d["v_cache"].clone()
+    try:
+        pkv.set_workspace(big)
+        out = pkv.decode_step(d["q"], k_new, v_new, kc2, vc2, d["block_tables"], d["context_lens"],
+                              w.scale, max_context_len=w.max_context_len)
+        torch.cuda.synchronize()
+    finally:
+        pkv.set_workspace(None)
+    assert pkv.get_device_error() == 0
+    for a_, b_ in ((out, ref), (kc2, kc1), (vc2, vc1)):
+        assert torch.equal(a_.view(torch.int16), b_.view(torch.int16))
