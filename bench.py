@@ -16,7 +16,9 @@ over a 16384-block pool), with seeded synthetic inputs.
 
 Prints ONE JSON line (rank 0).  `value` is decode-attention KV-read GB/s of the
 whole job: algorithmic K+V bytes (sum_i L_i * Hkv * D * 2 * 2 per step, all
-ranks) / max-over-ranks time of the timed steps.
+ranks) / max-over-ranks time of the timed steps.  The line's `workloads` object
+holds the same step measured on the other workloads (tiny MHA, Llama-3-8B GQA,
+long-context GQA, continuous batching with its two-call append time).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
     (N > 1: launch under torch.distributed.run; every rank runs an
@@ -504,7 +506,7 @@ def run_reference(args):
                    "head_dim": spec.head_dim, "block_size": spec.block_size,
                    "element_type": DTYPE_NAME[spec.dtype], "seed": args.seed},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "per step: " + desc},
+                         "sample": "per step: " + desc, **host_cpu()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
