@@ -83,3 +83,31 @@ def test_unique_bytes_count_shared_prefix_blocks_once():
     plain = W.make(W.scaled(W.WORKLOADS["llama7b_mha"], 4, 300), seed=0)
     assert plain.unique_kv_bytes() == plain.kv_bytes()     # nothing shared
     assert np.all(plain.context_lens >= 1)
+
+
+def test_host_cpu_description():
+    """The CPU baseline states the host it ran on: logical CPUs and a model."""
+    h = bench.host_cpu()
+    assert h["nproc"] is not None and h["nproc"] >= 1
+    assert set(h) == {"nproc", "cpu_model", "machine"}
+    assert h["machine"]
+
+
+def test_committed_traffic_record_is_consistent():
+    """profiles/decode_traffic.json, when it was taken on the kernel sources
+    as they are (else the benchmark reports no traffic), gives DRAM bytes
+    just above each workload's algorithmic bytes (unique bytes for the
+    continuous-batching batch, whose shared blocks L2 serves)."""
+    import pytest
+    for name in ("llama7b_mha", "llama3_8b_gqa", "long_ctx_gqa", "cont_batch"):
+        t = bench.recorded_traffic(name)
+        if t is None:
+            pytest.skip("the traffic record predates the current kernel sources")
+        # the seed-0 batch's lengths and tables, without drawing its pools
+        spec = W.WORKLOADS[name]
+        rng = np.random.default_rng([0, W.ORDER.index(name)])
+        lens = W.context_lengths(spec, rng)
+        tables, used = W.block_tables(spec, lens, rng)
+        w = W.Workload(spec, 0, lens, tables, None, used, None, None, None, None, None)
+        ref = w.unique_kv_bytes() if name == "cont_batch" else w.kv_bytes()
+        assert 1.0 <= t / ref < 1.05, (name, t / ref)
