@@ -357,6 +357,8 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
   plan->num_splits = static_cast<int32_t>((maxL + P - 1) / P);
   const long long grid = units * plan->num_splits;
   if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  // output rows (sequence, query head) are indexed in 32 bits by the reduce
+  if (static_cast<long long>(s->num_seqs) * s->num_q_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   plan->grid_ctas = static_cast<int32_t>(grid);
   plan->workspace_bytes =
       plan->num_splits > 1

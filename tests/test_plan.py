@@ -152,6 +152,8 @@ def test_tcgen05_plans(lib):
     (dict(num_q_heads=8, num_kv_heads=2, kernel=1), ERR_UNSUPPORTED),  # CUDA cores, group 4
     (dict(head_dim=64, kernel=3), ERR_UNSUPPORTED),            # tcgen05 needs head_dim 128
     (dict(split_tokens=-1), ERR_INVALID),                       # no persistent schedule
+    (dict(num_seqs=(1 << 26) + 1, num_q_heads=32, num_kv_heads=1,
+          max_context_len=16), ERR_UNSUPPORTED),                # 2^31 + 32 output rows
     (dict(max_context_len=100, max_blocks_per_seq=4), ERR_INVALID),  # > MB * bs
 ])
 def test_rejected_shapes(lib, kw, code):
