@@ -17,7 +17,8 @@
 //                          [NB, Hkv, bs, D] cache) into a ring of NS stages,
 //                          completing on per-stage mbarriers, 128-byte
 //                          swizzled so that the fragment reads below are
-//                          bank-conflict free
+//                          bank-conflict free, marked evict-first in L2
+//                          (each K/V row is read once per step)
 //   QK + online softmax -> FP32 logits in log2 units, running max m and sum l
 //   PV accumulate       -> FP32 output accumulators rescaled by 2^(m_old-m_new)
 // The warps of a CTA then merge their (m, l, o) in shared memory; the CTA
@@ -458,6 +459,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const uint32_t wbuf = smem_u32(smem + warp * NS * STAGE);
   const uint32_t wbar = smem_u32(&bars[warp * NS]);
 
+  const uint64_t policy = l2_policy_evict_first();   // the KV stream is read once
   auto issue = [&](int k) {
     const int st = k % NS;
     const int p = ids[warp + NW * k];
@@ -467,8 +469,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     mbar_arrive_expect_tx(bar, STAGE);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
-      tma_load_2d(dk + c * BS * 128, &tmK, c * 64, y, bar);
-      tma_load_2d(dk + TILE + c * BS * 128, &tmV, c * 64, y, bar);
+      tma_load_2d(dk + c * BS * 128, &tmK, c * 64, y, bar, policy);
+      tma_load_2d(dk + TILE + c * BS * 128, &tmV, c * 64, y, bar, policy);
     }
   };
   if (lane == 0) {

@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
   if (warp == LY::SOFT_WARPS) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();   // the KV stream is read once
       const int ntiles = 2 * ngroups;
       int t = 0;
       for (; t < ntiles; ++t) {
@@ -213,8 +214,8 @@ __global__ void __launch_bounds__(TcLayout<N>::THREADS, N > 16 ? 1 : 2)
         for (int b = 0; b < nb; ++b) {
           const int y = (ids[b0 + b] * a.Hkv + kvh) * BS;
           const uint32_t dst = sb + slot * LY::TILE + b * BS * 128;
-          tma_load_2d(dst, map, 0, y, full);
-          tma_load_2d(dst + 16384, map, 64, y, full);
+          tma_load_2d(dst, map, 0, y, full, policy);
+          tma_load_2d(dst + 16384, map, 64, y, full, policy);
         }
       }
       // every slot's last issued load lands before the CTA may exit (the
