@@ -115,7 +115,9 @@ typedef struct {
  * partition is 1024 tokens (2048 for the 16- and 32-head mma.sync tiles,
  * 2048/4096 for the tcgen05 kernel with 16/32 padded heads), or one wave of
  * equal partitions when the grid would be under four waves (two for the wide
- * mma.sync tiles). */
+ * mma.sync tiles); a wave is every CTA the SMs hold, or two per SM for the
+ * two-warp CTAs of 16 KB stages (head_dim 128 with block size 32, head_dim
+ * 256 with block size 16). */
 typedef struct {
   int32_t schedule;         /* always 0 (the partition schedule) */
   int32_t split_tokens;     /* P, tokens per partition */

@@ -339,10 +339,18 @@ int make_plan(const pkv_shape* s, int sms, pkv_plan* plan) {
     else
       P = wide_mma ? 2048 : 1024;
     // one wave when the grid would be under four waves (two for the wide
-    // mma.sync tiles, which measured faster at 3.4 waves than at one)
+    // mma.sync tiles, which measured faster at 3.4 waves than at one).  The
+    // two-warp CTAs of 16 KB stages fill that wave at two CTAs per SM, the
+    // others at every CTA an SM holds: measured on one GB300, the 4 x 32768
+    // long-context batch ran 1.2% faster at two (288 CTAs) than at three (448),
+    // a 2-sequence cut of it 4% faster, while the four-warp CTAs of 8 KB stages
+    // ran 15-18% slower at two.
     const long long min_waves = wide_mma ? 2 : 4;
     if (units > 0 && units * ((maxL + P - 1) / P) < min_waves * slots) {
-      const long long S = slots / units > 0 ? slots / units : 1;
+      const long long wave =
+          plan->variant != 2 && geo.warps == 2 && ctas_per_sm_for(geo.smem_bytes) > 2 ? 2LL * sms
+                                                                                   : slots;
+      const long long S = wave / units > 0 ? wave / units : 1;
       P = (maxL + S - 1) / S;
     }
     P = (P + gran - 1) / gran * gran;

@@ -75,9 +75,12 @@ def expected_plan(B_, Hq, Hkv, D, bs, maxL, split, sms):
     else:
         wide = variant == 1 and G > 8
         P = 2048 if wide else 1024
-        slots = sms * ctas_per_sm(smem(D, bs, nh))
+        cps = ctas_per_sm(smem(D, bs, nh))
+        slots = sms * cps
         if units > 0 and units * -(-maxL // P) < (2 if wide else 4) * slots:
-            S = max(slots // units, 1)
+            # one wave; the two-warp CTAs (16 KB stages) fill it at two per SM
+            wave = 2 * sms if nw == 2 and cps > 2 else slots
+            S = max(wave // units, 1)
             P = -(-maxL // S)
         P = -(-P // gran) * gran
         pmin = -(-maxL // 1024)                 # at most 1024 partitions per sequence
@@ -107,7 +110,7 @@ def test_benchmark_workload_plans(lib):
     want = {  # workload: (variant, P, S, grid)
         "llama7b_mha": (0, 1024, 4, 64 * 32 * 4),
         "llama3_8b_gqa": (1, 1024, 8, 128 * 8 * 8),
-        "long_ctx_gqa": (1, 2368, 14, 4 * 8 * 14),       # one wave of 448 CTAs
+        "long_ctx_gqa": (1, 3648, 9, 4 * 8 * 9),         # one wave at two CTAs per SM
         "cont_batch": (1, 1024, 2, 256 * 8 * 2),
         "tiny_mha": (0, 64, 4, 4 * 8 * 4),               # one wave, rounded to the 64-token grain
         "wide_gqa16": (1, 2048, 2, 64 * 8 * 2),
