@@ -199,17 +199,35 @@ int get_encoder() {
 // The pool [NB, Hkv, bs, D] as a 2-D tensor of NB * Hkv * bs rows of D
 // elements; one box is 64 elements (128 bytes) x bs rows with the 128-byte
 // swizzle, so one [bs, D] tile is D / 64 boxes.
-int encode_cache_map(CUtensorMap* map, const void* base, const pkv_shape& s) {
+// The cache [NB * Hkv * bs rows][D] seen as 64-element column boxes of bs
+// rows, 128-byte swizzled.  Two forms: 2-D (x = column, y = row; one box per
+// load, for the tcgen05 kernel, whose tiles keep the column boxes of 128
+// tokens apart) and 3-D (x = column within a box, y = row, z = box: a load
+// of one block's tile brings its D / 64 column boxes one after the other, as
+// the partition kernel stages them).
+int encode_cache_map(CUtensorMap* map, const void* base, const pkv_shape& s, bool three_d) {
   const cuuint64_t rows = static_cast<cuuint64_t>(s.num_blocks) * s.num_kv_heads * s.block_size;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.head_dim), rows};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(s.block_size)};
-  cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(s.head_dim) * 2;
   const CUtensorMapDataType dt =
       s.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r;
+  if (three_d) {
+    cuuint64_t dims[3] = {64, rows, static_cast<cuuint64_t>(s.head_dim / 64)};
+    cuuint64_t strides[2] = {row_bytes, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(s.block_size),
+                         static_cast<cuuint32_t>(s.head_dim / 64)};
+    r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.head_dim), rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(s.block_size)};
+    r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -217,18 +235,20 @@ struct MapCacheEntry {
   const void* base = nullptr;
   pkv_shape shape{};
   int device = -1;
+  bool three_d = false;
   CUtensorMap map{};
 };
 std::mutex g_map_mutex;
 MapCacheEntry g_map_cache[8];
 int g_map_next = 0;
 
-int cache_map(CUtensorMap* out, const void* base, const pkv_shape& s) {
+int cache_map(CUtensorMap* out, const void* base, const pkv_shape& s, bool three_d) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_map_mutex);
   for (auto& e : g_map_cache) {
-    if (e.base == base && e.device == dev && e.shape.num_blocks == s.num_blocks &&
+    if (e.base == base && e.device == dev && e.three_d == three_d &&
+        e.shape.num_blocks == s.num_blocks &&
         e.shape.num_kv_heads == s.num_kv_heads && e.shape.block_size == s.block_size &&
         e.shape.head_dim == s.head_dim && e.shape.dtype == s.dtype) {
       *out = e.map;
@@ -237,7 +257,7 @@ int cache_map(CUtensorMap* out, const void* base, const pkv_shape& s) {
   }
   MapCacheEntry& e = g_map_cache[g_map_next];
   g_map_next = (g_map_next + 1) % 8;
-  int rc = encode_cache_map(&e.map, base, s);
+  int rc = encode_cache_map(&e.map, base, s, three_d);
   if (rc != PKV_OK) {
     e.base = nullptr;
     return rc;
@@ -245,6 +265,7 @@ int cache_map(CUtensorMap* out, const void* base, const pkv_shape& s) {
   e.base = base;
   e.shape = s;
   e.device = dev;
+  e.three_d = three_d;
   *out = e.map;
   return PKV_OK;
 }
@@ -527,9 +548,10 @@ int decode_impl(const pkv_shape* s, const void* q, const void* k_cache, const vo
   rc = get_encoder();
   if (rc != PKV_OK) return rc;
   CUtensorMap tk, tv;
-  rc = cache_map(&tk, k_cache, *s);
+  const bool three_d = plan.variant != 2;
+  rc = cache_map(&tk, k_cache, *s, three_d);
   if (rc != PKV_OK) return rc;
-  rc = cache_map(&tv, v_cache, *s);
+  rc = cache_map(&tv, v_cache, *s, three_d);
   if (rc != PKV_OK) return rc;
 
   DecodeArgs a{};

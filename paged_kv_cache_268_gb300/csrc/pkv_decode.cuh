@@ -390,7 +390,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         const __grid_constant__ CUtensorMap tmV) {
   constexpr int TILE = BS * D * 2;
   constexpr int STAGE = 2 * TILE;
-  constexpr int CH = D / 64;
   constexpr int NH = Compute::NH;
   // The warps' final (m, l, o) merge reuses the ring; barriers and block ids
   // sit after whichever of the two is larger.
@@ -467,11 +466,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const uint32_t bar = wbar + 8 * st;
     const uint32_t dk = wbuf + st * STAGE;
     mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      tma_load_2d(dk + c * BS * 128, &tmK, c * 64, y, bar, policy);
-      tma_load_2d(dk + TILE + c * BS * 128, &tmV, c * 64, y, bar, policy);
-    }
+    // one box per tile: its D/64 column boxes of BS rows land one after the
+    // other (the maps' third dimension steps through them)
+    tma_load_3d(dk, &tmK, 0, y, 0, bar, policy);
+    tma_load_3d(dk + TILE, &tmV, 0, y, 0, bar, policy);
   };
   if (lane == 0) {
     const int pro = my_n < NS ? my_n : NS;
