@@ -312,10 +312,11 @@ int pick_variant(const pkv_shape* s) {
     case 2: return 1;
     case 3: return tc_ok ? 2 : -1;
     default:
-      // Measured on GB300: mma.sync stays ahead of the tcgen05 kernel at every
-      // group size (fraction of HBM peak: 0.92 vs 0.61 at group 4, 0.89 vs
-      // 0.88 at 8 on the long-context batch, 0.75 vs 0.72 at 16, 0.54 vs 0.52
-      // at 32), so the library's choice never takes tcgen05.
+      // Measured on GB300 (whole step, steps back to back): mma.sync stays ahead of the
+      // tcgen05 kernel at every group size (Llama-3-8B-shaped batch, group 4:
+      // 114.7 vs 188.4 us; long context, group 8: 82.5 vs 84.2 us; 128/8
+      // heads: 104.1 vs 120.7 us; 256/8 heads: 143.3 vs 174.1 us), so the
+      // library's choice never takes tcgen05.
       return G <= 2 ? 0 : 1;
   }
 }
